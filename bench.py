@@ -1,0 +1,440 @@
+"""Benchmark: achieved HBM GB/s (and % of the GB300 bandwidth roofline) and us/call of
+the RMSNorm hot path at T=8192, H=4096, bf16.
+
+One step = forward + deterministic fused backward (main strip kernel + dW column
+reduce) + fused residual-add/RMSNorm/E4M3 1x128 block quant, each on its own seeded
+synthetic inputs of the headline shape, with L2 flushed (a 512 MiB write) before every
+op and each op timed with CUDA events on its stream (the pages' protocol: kernel time,
+cold L2, FlashInfer PR #5741 Performance; miles-ext-kernels PR #15 Performance).
+The bandwidth is the logical-byte model of the same pages divided by the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent replica on
+its own GPU (the path needs no exchange between GPUs); the value is the bytes of all
+ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and us/call, RMSNorm fwd+fused bwd"
+UNIT = "GB/s"
+T_MAIN, H_MAIN = 8192, 4096
+WORKLOAD = ("RMSNorm forward + fused dX/dW backward (deterministic) + fused residual-add/"
+            "RMSNorm/E4M3 1x128 block quant, T=8192 H=4096 bf16 (fp32 rstd, dW, scales)")
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["rmsn_bwd.cu", "rmsn_device.cuh"]
+
+
+# ---------------------------------------------------------------------------- helpers
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(local_ms: float, local_bytes: int, world: int):
+    """Max step time over ranks and total bytes of all ranks (the replicas' whole job)."""
+    if world == 1:
+        return local_ms, local_bytes
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: copy, burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+def _source_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "rmsnorm_fwd_bwd_persistent_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the backward (main + dW reduce) from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "bwd_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_digest") == _source_digest():
+            return int(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------- our arm
+class Step:
+    """Device buffers of one step at the headline shape (inputs resident in HBM)."""
+
+    def __init__(self, dev, seed=0):
+        import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+        self.rmsn = rmsn
+        c = wl.MAIN_BF16
+        self.x, self.dy, self.w = wl.fwd_bwd_inputs(c, dev, seed)
+        self.y = torch.empty_like(self.x)
+        self.rstd = torch.empty(c.T, device=dev)
+        self.dx = torch.empty_like(self.x)
+        self.dw = torch.empty(c.H, device=dev)
+        nws = rmsn.rmsnorm_bwd_workspace_bytes(c.T, c.H, False, dev)
+        self.ws = torch.empty(max(nws, 16), device=dev, dtype=torch.uint8)
+        f = wl.FUSED_QUANT_MAIN
+        self.fx, self.fres, self.fw = wl.fused_inputs(f, dev, seed + 1)
+        self.q = torch.empty(f.T, f.H, device=dev, dtype=torch.uint8)
+        self.scale = torch.empty(f.H // 128, wl.round_up(f.T, 4), device=dev)
+        self.normed = torch.empty_like(self.fx)
+        self.eps = c.eps
+        self.flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+        self.bytes = {
+            "fwd": wl.fwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype),
+            "bwd": wl.bwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype),
+            "fused_quant": wl.fused_quant_bytes(f.T, f.H),
+        }
+        # fwd writes rstd for the bwd once, so the bwd sees the forward's saved value
+        rmsn.rmsnorm_fwd(self.x, self.w, self.eps, y=self.y, rstd=self.rstd)
+
+    def fwd(self):
+        self.rmsn.rmsnorm_fwd(self.x, self.w, self.eps, y=self.y, rstd=self.rstd)
+
+    def bwd(self):
+        self.rmsn.rmsnorm_bwd(self.dy, self.x, self.w, self.rstd, deterministic=True,
+                              compensated=False, workspace=self.ws, dx=self.dx, dw=self.dw)
+
+    def fused(self):
+        self.rmsn.fused_add_rmsnorm_fp8_block_quant(self.fx, self.fres, self.fw, self.eps,
+                                                    q=self.q, block_scale=self.scale,
+                                                    normed=self.normed)
+
+    OPS = ("fwd", "bwd", "fused_quant")
+    LAUNCHES = {"fwd": 1, "bwd": 2, "fused_quant": 1}
+
+    def run_op(self, name):
+        {"fwd": self.fwd, "bwd": self.bwd, "fused_quant": self.fused}[name]()
+
+
+def time_steps(step: Step, steps: int, warmup: int, world: int):
+    ev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)] for op in Step.OPS}
+    for _ in range(warmup):
+        for op in Step.OPS:
+            step.flush.zero_()
+            step.run_op(op)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        for op in Step.OPS:
+            step.flush.zero_()  # L2 flush between timed ops (outside the events)
+            s, e = ev[op][i]
+            s.record()
+            step.run_op(op)
+            e.record()
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    per_op = {op: [s.elapsed_time(e) for s, e in ev[op]] for op in Step.OPS}
+    return per_op, wall
+
+
+def time_e2e(step: Step, steps: int, warmup: int):
+    """The same step through the public API from pinned host buffers: every step copies
+    its inputs host->device, runs the three ops and copies every output device->host."""
+    dev = step.x.device
+    ins = {k: getattr(step, k) for k in ("x", "dy", "w", "fx", "fres", "fw")}
+    outs = {k: getattr(step, k) for k in ("y", "rstd", "dx", "dw", "q", "scale", "normed", "fres")}
+    h_in = {k: v.cpu().pin_memory() for k, v in ins.items()}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def one():
+        for k, v in ins.items():
+            v.copy_(h_in[k], non_blocking=True)
+        step.fwd()
+        step.bwd()
+        step.fused()
+        for k, v in outs.items():
+            h_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    e.synchronize()
+    del dev
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+# --------------------------------------------------------------------- oracle legs
+def oracle_sample_step(rows: int, seed: int = 0):
+    """One pass of the FP64 oracle over `rows` rows of each op of the step (CPU)."""
+    import dataclasses
+    import oracle
+    c = dataclasses.replace(wl.MAIN_BF16, T=rows)
+    x, dy, w = wl.fwd_bwd_inputs(c, "cpu", seed)
+    f = dataclasses.replace(wl.FUSED_QUANT_MAIN, T=rows)
+    fx, fres, fw = wl.fused_inputs(f, "cpu", seed + 1)
+    X, DY, W = wl.to_oracle(x), wl.to_oracle(dy), wl.to_oracle(w)
+    FX, FR, FW = wl.to_oracle(fx), wl.to_oracle(fres), wl.to_oracle(fw)
+    nbytes = (wl.fwd_bytes(rows, c.H, c.x_dtype, c.w_dtype) +
+              wl.bwd_bytes(rows, c.H, c.x_dtype, c.w_dtype) + wl.fused_quant_bytes(rows, f.H))
+
+    def run():
+        _, r = oracle.rmsnorm_fwd(X, W, c.eps)
+        oracle.rmsnorm_bwd(DY, X, W, r)
+        _, n, _ = oracle.fused_add_rmsnorm(FX, FR, FW, f.eps)
+        nb = oracle.bf16_round(n).reshape(n.shape)
+        oracle.block_quant_e4m3(nb, wl.round_up(rows, 4))
+    return run, nbytes
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    import oracle
+    rows = 256
+    run, nbytes = oracle_sample_step(rows)
+    run()  # builds/loads the oracle
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        run()
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": nbytes * n / dt / 1e9, "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"{n} passes of the FP64 oracle over {rows} rows (H=4096) of each op of the "
+                      f"step: fwd, bwd (dx and dW), fused add+norm+E4M3 quant; {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    run, nbytes = oracle_sample_step(8)
+    run()
+    t = time.perf_counter()
+    run()
+    one = max(time.perf_counter() - t, 1e-4)
+    budget = 90.0 / max(args.steps + args.warmup, 1)
+    rows = int(max(8, min(2048, 8 * budget / one)))
+    run, nbytes = oracle_sample_step(rows)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    sample = (f"each step: the FP64 oracle over {rows} of the T=8192 rows (H=4096) of each op: "
+              f"fwd, bwd (dx and dW), fused add+norm+E4M3 quant")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; x, dy ~ N(0,1), residual ~ N(0,2), w = 1 + 0.1 N(0,1))",
+        "config": {"workload": WORKLOAD, "T": T_MAIN, "H": H_MAIN, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    step = Step(dev)
+    peak, peak_src = measured_peak()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    per_op, wall = time_steps(step, args.steps, args.warmup, world)
+    clk = clocks.stop()
+
+    op_ms = {op: statistics.mean(v) for op, v in per_op.items()}
+    step_ms = sum(op_ms.values())
+    step_bytes = sum(step.bytes.values())
+    max_ms, total_bytes = aggregate(step_ms, step_bytes, world)
+    value = total_bytes / (max_ms * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
+    e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
+    e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
+
+    ops = {}
+    for op in Step.OPS:
+        us = statistics.median(per_op[op]) * 1e3
+        gbs = step.bytes[op] / (op_ms[op] * 1e-3) / 1e9
+        ops[op] = {"us_median": us, "us_mean": op_ms[op] * 1e3, "gbs": gbs, "frac": gbs / peak,
+                   "bytes": step.bytes[op], "launches": Step.LAUNCHES[op]}
+    dom = max(Step.OPS, key=lambda o: op_ms[o])
+    achieved = step.bytes[dom] / (op_ms[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic() if dom == "bwd" else None
+
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; x, dy ~ N(0,1), residual ~ N(0,2), w = 1 + 0.1 N(0,1))",
+        "config": {"workload": WORKLOAD, "T": T_MAIN, "H": H_MAIN, "x_dtype": "bf16",
+                   "w_dtype": "bf16", "accumulate": "fp32", "bwd_mode": "deterministic",
+                   "l2": "flushed before every timed op (512 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "ops": ops,
+        "roofline": {"bound": "hbm", "kernel": {"bwd": "rmsnorm_bwd (main strip kernel + dW "
+                                                       "column reduce)",
+                                                "fwd": "rmsnorm_fwd_kernel",
+                                                "fused_quant": "fused_add_rmsnorm_fp8_kernel"}[dom],
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": step.bytes[dom],
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+        "gpu_launches": sum(Step.LAUNCHES.values()) * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

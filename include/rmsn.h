@@ -1,0 +1,216 @@
+/*
+ * rmsn.h -- C ABI of the GB300 (sm_103a) RMSNorm library.
+ *
+ * Three operations, each enqueued on a caller-provided CUDA stream:
+ *
+ *   rmsnorm_fwd                        y = x * rstd * w,  rstd = 1/sqrt(mean(x^2) + eps)
+ *   rmsnorm_bwd                        dx = rstd * (g - xhat * mean(g * xhat)),
+ *                                      dw = sum over rows of dy * xhat
+ *                                      (g = dy * w, xhat = x * rstd), one fused pass
+ *   fused_add_rmsnorm_fp8_block_quant  h = bf16(x + residual) -> residual (in place),
+ *                                      normed = bf16(h * rstd * w),
+ *                                      per 1x128 block: scale = amax/448,
+ *                                      q = e4m3(normed / scale)
+ *
+ * Sources (page title and section):
+ *   FlashInfer PR #5741 "cake_rmsnorm_train" (BF16 RMSNorm training forward and
+ *     one-launch backward): Design (Forward, Backward), API, Memory, Determinism,
+ *     Precision.
+ *   Liger-Kernel PR #1336 "perf(cutedsl): fused dX+dW backward + host-enqueue caching
+ *     for RMSNorm": Summary (fused single-pass dX+dW strip-reduction backward), review
+ *     (persistent CTAs, 16-byte copies, warps per token).
+ *   miles-ext-kernels PR #15 (re-vendoring the Cake RMSNorm packages): Changes
+ *     (deterministic package, TwoSum per-thread weight-gradient sums), Accuracy
+ *     (weight-gradient budget).
+ *   FlashInfer PR #4480 "Add FusedAddRMSNormFP8BlockQuant": Summary, Kernel, API.
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers only (except where stated); the caller allocates every buffer,
+ *     the library allocates nothing, never synchronizes the stream and keeps no
+ *     pointer after it returns.  All work is enqueued on `stream` (NULL = the legacy
+ *     default stream); completion is the caller's to observe.
+ *   - [T, H] tensors are row-major and contiguous (row stride H elements).  Every
+ *     [T, H] / [H] base pointer must be 16-byte aligned.  H must be a multiple of 8 for
+ *     bf16 and of 4 for fp32 tensors (16-byte vectors) and at most RMSN_MAX_H.
+ *   - Arguments are checked before anything is enqueued; a failed check returns a
+ *     status and enqueues nothing.  A launch failure returns RMSN_ERR_CUDA.  Errors that
+ *     the stream reports later (asynchronously) are the caller's to observe.
+ *   - T == 0 is valid and enqueues no kernel (rmsnorm_bwd still zeroes dw).
+ *   - Arithmetic: FP32 statistics and reductions, IEEE division and square root, no
+ *     fast-math; bf16 outputs are rounded once, to nearest even.
+ */
+#ifndef RMSN_H_
+#define RMSN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Stream handle; the same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* rmsn_stream_t;
+
+/* Element types of x / dy / y / dx and of w. */
+typedef enum {
+    RMSN_F32 = 0,  /* IEEE binary32 */
+    RMSN_BF16 = 1  /* bfloat16 */
+} rmsn_dtype;
+
+typedef enum {
+    RMSN_OK = 0,
+    RMSN_ERR_INVALID_ARG = 1,         /* NULL pointer, bad dtype code, T < 0, bad eps */
+    RMSN_ERR_UNSUPPORTED_SHAPE = 2,   /* H out of range or not a multiple of the vector */
+    RMSN_ERR_MISALIGNED = 3,          /* a pointer violates its alignment */
+    RMSN_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace smaller than rmsnorm_bwd_workspace_bytes */
+    RMSN_ERR_CUDA = 5                 /* a CUDA runtime call or a launch failed */
+} rmsn_status;
+
+#define RMSN_MAX_H 16384
+
+/* Human-readable text of a status code (static storage; never NULL). */
+const char* rmsn_status_string(int status);
+
+/* ------------------------------------------------------------------------------------
+ * rmsnorm_fwd -- RMSNorm forward; saves the FP32 reciprocal RMS for the backward.
+ *
+ * Source: FlashInfer PR #5741 "cake_rmsnorm_train", Design/Forward: FP32 sum of squares,
+ * IEEE rsqrt in FP32, one pass that writes y = bf16(x * rstd * w) and the FP32 rstd;
+ * API: cake_rmsnorm_train_forward(x, w, eps) -> (y, rstd).
+ *
+ *   x     [T, H] in x_dtype (device, read)
+ *   w     [H] in w_dtype (device, read)
+ *   y     [T, H] in x_dtype (device, written); y_ij = round(x_ij * rstd_i * w_j),
+ *         the product formed in FP32 left to right and rounded once
+ *   rstd  [T] fp32 (device, written); rstd_i = 1 / sqrt(sum_j x_ij^2 / H + eps)
+ *   eps   finite, >= 0 (with eps == 0 an all-zero row gives rstd = inf)
+ * Returns RMSN_OK or an error status (see conventions).
+ * ---------------------------------------------------------------------------------- */
+int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y, float* rstd,
+                int64_t T, int64_t H, float eps, rmsn_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * rmsnorm_bwd_workspace_bytes -- size of the scratch buffer rmsnorm_bwd needs.
+ *
+ * Source: FlashInfer PR #5741, API (backward workspace query; caller-owned, reusable
+ * across T) and Memory (per-chunk FP32 partials of dw).
+ *
+ * The workspace holds one FP32 partial row of dw per row chunk (two rows, high and low
+ * part, when `compensated` is set).  The value returned for (T, H) is an upper bound
+ * for every T' <= T with the same H, compensated flag and device, so one buffer can
+ * be reused across calls.  `device` is a CUDA device ordinal (its SM count decides
+ * the number of chunks).  Returns 0 for T <= 0, for an unsupported H, or when the
+ * device cannot be queried.
+ * ---------------------------------------------------------------------------------- */
+size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int device);
+
+/* ------------------------------------------------------------------------------------
+ * rmsnorm_bwd -- fused single-pass RMSNorm backward: dx and dw together.
+ *
+ * Sources: FlashInfer PR #5741, Design/Backward: a persistent grid over static row
+ * chunks; each CTA writes dx for its rows, dx = rstd * (g*w - mean(g*w*xhat) * xhat) in
+ * FP32, and keeps an FP32 dw partial for its chunk; the partials are then reduced per
+ * column in chunk order, without atomics.  Liger-Kernel PR #1336, Summary: the fused
+ * dX+dW strip-reduction backward.  miles-ext-kernels PR #15, Changes: the
+ * deterministic ("det") and non-deterministic ("fast") backward, and TwoSum per-thread
+ * weight-gradient sums.
+ *
+ *   dy    [T, H] in x_dtype (device, read)
+ *   x     [T, H] in x_dtype (device, read): the forward's input
+ *   w     [H] in w_dtype (device, read)
+ *   rstd  [T] fp32 (device, read): the forward's saved rstd
+ *   dx    [T, H] in x_dtype (device, written)
+ *   dw    [H] fp32 (device, written, overwritten -- not accumulated into)
+ *   deterministic  != 0: per-chunk partials go to the workspace and a second kernel
+ *         folds them per column in a fixed order; dw is bitwise reproducible and a
+ *         function of (T, H, dtypes, compensated, the device's SM count) only.
+ *         == 0: dw is zeroed and the partials are added with FP32 atomics (no second
+ *         kernel, no workspace; bits may differ from run to run).
+ *   compensated  != 0: every dw partial is an FP32 (high, low) pair summed with the
+ *         error-free TwoSum transformation, through the chunk fold and the column
+ *         reduction; dw = high + low rounded once.
+ *   workspace, workspace_bytes  device scratch of at least
+ *         rmsnorm_bwd_workspace_bytes(T, H, compensated, device) bytes, 16-byte
+ *         aligned; its contents on entry do not matter and on exit are unspecified.
+ *         Needed when deterministic != 0; may be NULL / 0 otherwise.
+ * Returns RMSN_OK or an error status (see conventions).
+ * ---------------------------------------------------------------------------------- */
+int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w_dtype,
+                const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
+                int deterministic, int compensated, void* workspace, size_t workspace_bytes,
+                rmsn_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * fused_add_rmsnorm_fp8_block_quant -- residual add + RMSNorm + E4M3 1x128 block
+ * quantization in one pass.
+ *
+ * Source: FlashInfer PR #4480 "Add FusedAddRMSNormFP8BlockQuant", Summary and Kernel:
+ * emits the fp8 activation, one fp32 scale per 1x128 block in the column-major
+ * (H/128, round_up(T, 4)) layout consumed by block-scaled fp8 GEMMs, the pre-norm
+ * residual in place and the bf16 normed output; the fp8 is quantized from the
+ * bf16-rounded normed value, so re-quantizing `normed` reproduces `q` exactly; a
+ * block's amax is a register-only shuffle among the lanes that hold it.  API: the
+ * caller allocates every output, residual is updated in place.
+ *
+ *   x         [T, H] bf16 (device, read)
+ *   residual  [T, H] bf16 (device, read and written): residual_ij <- h_ij = bf16(x_ij + residual_ij)
+ *   w         [H] bf16 (device, read)
+ *   q         [T, H] E4M3 codes, one byte each (device, written):
+ *             q_ij = e4m3_rn_satfinite(n_ij / scale_ib) with n = normed; if a block's
+ *             amax is 0 its scale is 0 and q holds the signed zero of each element
+ *   block_scale  fp32 (device, written): scale of (row m, block b = column/128) at
+ *             block_scale[b * scale_ld + m], i.e. an (H/128, scale_ld) row-major buffer,
+ *             unit stride along the rows; scale = amax_b(|n|) / 448 in IEEE FP32.
+ *             Entries with m >= T are not written.
+ *   scale_ld  >= round_up(T, 4)
+ *   normed    [T, H] bf16 (device, written): n_ij = bf16(h_ij * rstd_i * w_j),
+ *             rstd_i = 1/sqrt(mean_j h_ij^2 + eps)
+ *   H         multiple of 128, at most RMSN_MAX_H
+ * Alignment: x, residual, w, normed, q 16 bytes; block_scale 4 bytes.
+ * Returns RMSN_OK or an error status (see conventions).
+ * ---------------------------------------------------------------------------------- */
+int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void* w,
+                                      uint8_t* q, float* block_scale, int64_t scale_ld,
+                                      void* normed, int64_t T, int64_t H, float eps,
+                                      rmsn_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Launch policy (introspection).  The geometry the library uses for a call, computed
+ * on the host without a GPU; `sm_count` is the device's multiprocessor count.
+ *
+ * Source: Liger-Kernel PR #1336, Summary and review (fast-path eligibility as a pure
+ * host function of the shape: vector width and warp count; persistent CTAs; several
+ * warps per token row).
+ * ---------------------------------------------------------------------------------- */
+typedef enum { RMSN_OP_FWD = 0, RMSN_OP_BWD = 1, RMSN_OP_FUSED_QUANT = 2 } rmsn_op;
+
+typedef struct {
+    int vec_elems;        /* elements per 16-byte vector */
+    int warps_per_row;    /* warps that share one row */
+    int chunks_per_lane;  /* 16-byte vectors each lane holds per row (compile-time) */
+    int threads;          /* threads per CTA */
+    int rows_per_cta;     /* rows a CTA works on at once (threads / (32*warps_per_row)) */
+    int ctas_per_sm;      /* CTAs per SM the persistent grid is sized for */
+    int64_t grid;         /* CTAs launched (for the backward: the number of row chunks) */
+    int64_t smem_bytes;   /* dynamic shared memory per CTA */
+    int64_t workspace_bytes; /* backward scratch (0 for the other ops) */
+} rmsn_plan_t;
+
+/* Fills *out for (op, T, H, dtypes, compensated) on a device with `sm_count` SMs.
+ * Returns RMSN_OK, or the status the corresponding entry point would return for an
+ * unsupported shape or dtype. */
+int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compensated,
+              int sm_count, rmsn_plan_t* out);
+
+/* Tuning hook for benchmarks: overrides the default threads per CTA, CTAs per SM and
+ * warps per row of one op for the whole process (0 keeps a default).  Changing it while
+ * calls are in flight on other host threads is a race.  Returns RMSN_ERR_INVALID_ARG for
+ * a combination the kernels cannot run (then nothing changes). */
+int rmsn_set_policy(int op, int threads, int ctas_per_sm, int warps_per_row);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSN_H_ */

@@ -56,6 +56,8 @@ def lib():
             L = ctypes.CDLL(build())
             L.or_bf16_round.restype = ctypes.c_uint16
             L.or_bf16_round.argtypes = [ctypes.c_double]
+            L.or_bf16_round_n.restype = None
+            L.or_bf16_round_n.argtypes = [_vp, _i64, _vp]
             L.or_e4m3_encode.restype = ctypes.c_uint8
             L.or_e4m3_encode.argtypes = [ctypes.c_float]
             L.or_e4m3_decode.restype = ctypes.c_float
@@ -175,9 +177,10 @@ def block_quant_e4m3(n_bits: np.ndarray, ld: int, scale_init: np.ndarray | None 
 # -------------------------------------------------------------------- scalar codecs
 def bf16_round(values) -> np.ndarray:
     """Round binary64 values to bf16 (nearest, ties to even); returns bit patterns."""
-    v = np.asarray(values, dtype=np.float64).reshape(-1)
-    L = lib()
-    return np.array([L.or_bf16_round(float(a)) for a in v], dtype=np.uint16)
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64).reshape(-1))
+    out = np.empty(v.shape, np.uint16)
+    lib().or_bf16_round_n(_ptr(v), v.size, _ptr(out))
+    return out
 
 
 def e4m3_encode(values) -> np.ndarray:

@@ -90,6 +90,12 @@ uint16_t or_bf16_round(double d)
     return bits;
 }
 
+/* or_bf16_round over an array */
+void or_bf16_round_n(const double* v, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_round(v[i]);
+}
+
 /* OCP E4M3 ("FN") decode of one code, exact in binary32 */
 float or_e4m3_decode(uint8_t code)
 {

@@ -1,0 +1,143 @@
+"""Parity checks of the CUDA path against the FP64 oracle (helpers for the GPU tests).
+
+Outputs are NaN-poisoned before each call (an element the kernel leaves unwritten
+fails the gate) and sit inside guard bands filled with a sentinel (a write outside the
+output fails the guard check).  Large cases compare a sample of rows elementwise and
+the whole weight gradient.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import gates
+import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+import workloads as wl
+
+GUARD = 64  # elements of guard band on each side (a multiple of 16 bytes for any dtype)
+FULL_LIMIT = 1 << 25  # compare every element up to this many; sample rows above
+
+
+def guarded(shape, dtype, device, fill=float("nan")):
+    """A contiguous tensor of `shape` inside a buffer with GUARD sentinel elements around it."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    buf = torch.empty(n + 2 * GUARD, dtype=dtype, device=device)
+    if dtype == torch.uint8:
+        buf.fill_(0xA5)
+    else:
+        buf.fill_(-12288.0)
+    body = buf[GUARD:GUARD + n].view(*shape)
+    if dtype == torch.uint8:
+        body.fill_(0xFF)  # E4M3 NaN code: any unwritten byte fails
+    else:
+        body.fill_(fill)
+    return buf, body
+
+
+def guards_ok(buf: torch.Tensor) -> bool:
+    g = torch.cat([buf[:GUARD], buf[-GUARD:]])
+    if buf.dtype == torch.uint8:
+        return bool((g == 0xA5).all())
+    return bool((g == -12288.0).all())
+
+
+def _rows(T: int, H: int, nsample: int = 192, seed: int = 0) -> np.ndarray:
+    if T * H <= FULL_LIMIT:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(T, size=min(nsample, T), replace=False)
+    return np.unique(np.concatenate([pick, [0, 1, T - 2, T - 1]]))
+
+
+def _f64(a: np.ndarray) -> np.ndarray:
+    return oracle.bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def check_fwd(x: torch.Tensor, w: torch.Tensor, eps: float) -> dict:
+    T, H = x.shape
+    ybuf, y = guarded((T, H), x.dtype, x.device)
+    rbuf, rstd = guarded((T,), torch.float32, x.device)
+    rmsn.rmsnorm_fwd(x, w, eps, y=y, rstd=rstd)
+    torch.cuda.synchronize()
+    rows = _rows(T, H)
+    X = wl.to_oracle(x[torch.from_numpy(rows).to(x.device)])
+    W = wl.to_oracle(w)
+    y_ref, r_ref = oracle.rmsnorm_fwd(X, W, eps)
+    y_dev = wl.to_oracle(y[torch.from_numpy(rows).to(x.device)])
+    r_dev = rstd.cpu().numpy()[rows]
+    out = {"rstd": gates.check_f32_rel(r_dev, r_ref)}
+    if x.dtype == torch.bfloat16:
+        out["y"] = gates.check_bf16(y_dev, y_ref)
+    else:
+        out["y"] = gates.check_f32_rel(y_dev, y_ref)
+    out["guards"] = {"n_fail": int(not (guards_ok(ybuf) and guards_ok(rbuf)))}
+    out["_rstd_dev"] = rstd
+    return out
+
+
+def check_bwd(dy, x, w, rstd, deterministic=True, compensated=False, full_dw=True,
+              workspace=None) -> dict:
+    T, H = x.shape
+    dxbuf, dx = guarded((T, H), x.dtype, x.device)
+    dwbuf, dw = guarded((H,), torch.float32, x.device)
+    if deterministic and workspace is None:
+        n = rmsn.rmsnorm_bwd_workspace_bytes(T, H, compensated, x.device)
+        workspace = torch.full((max(n, 16) // 4,), float("nan"), device=x.device,
+                               dtype=torch.float32)
+    rmsn.rmsnorm_bwd(dy, x, w, rstd, deterministic=deterministic, compensated=compensated,
+                     workspace=workspace, dx=dx, dw=dw)
+    torch.cuda.synchronize()
+    rows = _rows(T, H)
+    ridx = torch.from_numpy(rows).to(x.device)
+    W = wl.to_oracle(w)
+    r_all = rstd.cpu().numpy().astype(np.float64)
+    DYs, Xs = wl.to_oracle(dy[ridx]), wl.to_oracle(x[ridx])
+    dx_ref, _ = oracle.rmsnorm_bwd(DYs, Xs, W, r_all[rows], want_dw=False)
+    dx_dev = wl.to_oracle(dx[ridx])
+    out = {}
+    if x.dtype == torch.bfloat16:
+        extra = gates.dx_fp32_bound(_f64(DYs), _f64(Xs), _f64(W), r_all[rows], dx_ref)
+        out["dx"] = gates.check_bf16(dx_dev, dx_ref, extra=extra)
+    else:
+        out["dx"] = gates.check_f32_rel(dx_dev, dx_ref, row_rms_term=True)
+    if full_dw:
+        _, dw_ref = oracle.rmsnorm_bwd(wl.to_oracle(dy), wl.to_oracle(x), W, r_all, want_dx=False)
+        out["dw"] = gates.check_dw(dw.cpu().numpy(), dw_ref)
+    out["guards"] = {"n_fail": int(not (guards_ok(dxbuf) and guards_ok(dwbuf)))}
+    out["_dw_dev"] = dw
+    return out
+
+
+def check_fused(x, res, w, eps, ld_pad: int = 0) -> dict:
+    T, H = x.shape
+    ld = wl.round_up(T, 4) + ld_pad
+    res_in = wl.to_oracle(res).copy()
+    qbuf, q = guarded((T, H), torch.uint8, x.device)
+    sbuf, scale = guarded((H // 128, ld), torch.float32, x.device)
+    nbuf, normed = guarded((T, H), torch.bfloat16, x.device)
+    rmsn.fused_add_rmsnorm_fp8_block_quant(x, res, w, eps, q=q, block_scale=scale, normed=normed)
+    torch.cuda.synchronize()
+    h_ref, n_ref, _ = oracle.fused_add_rmsnorm(wl.to_oracle(x), res_in, wl.to_oracle(w), eps)
+    nb = wl.to_oracle(normed)
+    s_dev = scale.cpu().numpy().reshape(-1)
+    q_ref, s_ref = oracle.block_quant_e4m3(nb, ld)
+    valid = np.zeros((H // 128, ld), bool)
+    valid[:, :T] = True
+    valid = valid.reshape(-1)
+    out = {
+        "residual": {"n_fail": int(np.count_nonzero(wl.to_oracle(res) != h_ref))},
+        "normed": gates.check_bf16(nb, n_ref),
+        "q": {"n_fail": int(np.count_nonzero(q.cpu().numpy() != q_ref))},
+        "scale": {"n_fail": int(np.count_nonzero(s_dev[valid].view(np.uint32) !=
+                                                 s_ref[valid].view(np.uint32)))},
+        # pad entries m in [T, ld) keep the poison (NaN) the test wrote
+        "scale_pads": {"n_fail": int(np.count_nonzero(~np.isnan(s_dev[~valid])))},
+        "guards": {"n_fail": int(not (guards_ok(qbuf) and guards_ok(sbuf) and guards_ok(nbuf)))},
+    }
+    return out
+
+
+def assert_ok(res: dict, what: str = ""):
+    bad = {k: v for k, v in res.items() if not k.startswith("_") and v.get("n_fail")}
+    assert not bad, f"{what}: parity failed: {bad}"

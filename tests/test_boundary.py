@@ -1,0 +1,168 @@
+"""The C ABI without a GPU: the library loads and exports every function include/rmsn.h
+declares; argument checks return their status before anything touches CUDA; the
+launch planner (a pure host function) covers each row exactly and sizes the backward
+workspace as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+from rmsnorm_fwd_bwd_persistent_gb300 import build as rbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rmsn.h")
+
+OK, INVALID, SHAPE, MISALIGNED, WS_SMALL, CUDA = 0, 1, 2, 3, 4, 5
+A = 1 << 20  # a fake, 16-byte aligned "device" address: never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rbuild.build()
+    return rmsn.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert {"rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
+            "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan",
+            "rmsn_set_policy"} <= set(names)
+    raw = ctypes.CDLL(rmsn.library_path())
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in rmsn.h but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(0, 6):
+        assert rmsn.rmsn_status_string(s) and rmsn.rmsn_status_string(s) != "unknown status"
+    assert rmsn.rmsn_status_string(99) == "unknown status"
+
+
+def test_fwd_argument_checks(lib):
+    f = lib.rmsnorm_fwd
+    assert f(A, 1, A, 1, A, A, 4, 7, 1e-6, None) == SHAPE          # H not a multiple of 8
+    assert f(A, 0, A, 0, A, A, 4, 6, 1e-6, None) == SHAPE          # fp32: H % 4
+    assert f(A, 1, A, 1, A, A, 4, 16392, 1e-6, None) == SHAPE      # above the maximum
+    assert f(A, 1, A, 1, A, A, 4, 0, 1e-6, None) == SHAPE
+    assert f(A, 2, A, 1, A, A, 4, 64, 1e-6, None) == INVALID       # dtype code
+    assert f(A, 1, A, 1, A, A, -1, 64, 1e-6, None) == INVALID      # T < 0
+    assert f(A, 1, A, 1, A, A, 4, 64, float("nan"), None) == INVALID
+    assert f(A, 1, A, 1, A, A, 4, 64, -1.0, None) == INVALID
+    assert f(A, 1, A, 1, A, A, 4, 64, float("inf"), None) == INVALID
+    assert f(None, 1, A, 1, A, A, 4, 64, 1e-6, None) == INVALID
+    assert f(A + 8, 1, A, 1, A, A, 4, 64, 1e-6, None) == MISALIGNED
+    assert f(A, 1, A, 1, A + 4, A, 4, 64, 1e-6, None) == MISALIGNED
+    assert f(A, 1, A, 1, A, A + 2, 4, 64, 1e-6, None) == MISALIGNED
+    assert f(None, 1, None, 1, None, None, 0, 64, 1e-6, None) == OK   # T == 0: nothing to do
+
+
+def test_bwd_argument_checks(lib):
+    b = lib.rmsnorm_bwd
+    assert b(A, A, 1, A, 0, A, A, A, 4, 12, 1, 0, A, 1 << 20, None) == SHAPE
+    assert b(A, A, 1, A, 0, A, A, None, 4, 64, 1, 0, A, 1 << 20, None) == INVALID
+    assert b(A, A, 1, A, 0, A, A, A + 4, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
+    assert b(A, A, 3, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID
+    assert b(None, A, 1, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID
+    assert b(A, A + 2, 1, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
+
+
+def test_fused_argument_checks(lib):
+    f = lib.fused_add_rmsnorm_fp8_block_quant
+    assert f(A, A, A, A, A, 8, A, 8, 200, 1e-6, None) == SHAPE     # H % 128
+    assert f(A, A, A, A, A, 8, A, 8, 32768, 1e-6, None) == SHAPE   # above the maximum
+    assert f(A, A, A, A, A, 4, A, 7, 256, 1e-6, None) == INVALID   # ld < round_up(T, 4) = 8
+    assert f(A, A, A, A, A + 2, 8, A, 7, 256, 1e-6, None) == MISALIGNED
+    assert f(A, A, A, A + 8, A, 8, A, 7, 256, 1e-6, None) == MISALIGNED
+    assert f(A, None, A, A, A, 8, A, 7, 256, 1e-6, None) == INVALID
+    assert f(None, None, None, None, None, 0, None, 0, 256, 1e-6, None) == OK
+
+
+SM = 152
+
+
+@pytest.mark.parametrize("op", [rmsn.OP_FWD, rmsn.OP_BWD, rmsn.OP_FUSED_QUANT])
+@pytest.mark.parametrize("H", [8, 128, 256, 1536, 2048, 4096, 4104, 5120, 6144, 8192, 16384])
+@pytest.mark.parametrize("xd,wd", [(1, 1), (1, 0), (0, 0), (0, 1)])
+def test_plan_covers_rows(lib, op, H, xd, wd):
+    if op == rmsn.OP_FUSED_QUANT and (xd, wd) != (1, 1):
+        with pytest.raises(rmsn.RmsnError):
+            rmsn.rmsn_plan(op, 100, 4096, xd, wd)
+        return
+    vec = 8 if xd == 1 else 4
+    if H % vec or (op == rmsn.OP_FUSED_QUANT and H % 128):
+        with pytest.raises(rmsn.RmsnError):
+            rmsn.rmsn_plan(op, 100, H, xd, wd)
+        return
+    for T in (1, 65, 8192, 262144):
+        p = rmsn.rmsn_plan(op, T, H, xd, wd, sm_count=SM)
+        lanes = 32 * p["warps_per_row"]
+        assert p["vec_elems"] == vec
+        assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
+        assert p["threads"] % lanes == 0 and p["threads"] <= 512
+        assert p["rows_per_cta"] == p["threads"] // lanes
+        assert 1 <= p["grid"] <= SM * p["ctas_per_sm"]
+        assert p["grid"] <= -(-T // p["rows_per_cta"])              # no idle CTAs
+        if op == rmsn.OP_FUSED_QUANT:
+            assert lanes % 16 == 0                                  # 16 lanes hold one block
+
+
+def test_plan_headline_geometry(lib):
+    f = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
+    assert (f["warps_per_row"], f["chunks_per_lane"]) == (2, 8)
+    b = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1)
+    assert (b["warps_per_row"], b["chunks_per_lane"]) == (4, 4)
+    assert b["workspace_bytes"] == b["grid"] * 4096 * 4
+    bc = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1, compensated=True)
+    assert bc["workspace_bytes"] == 2 * bc["grid"] * 4096 * 4
+
+
+def test_workspace_grows_with_t(lib):
+    prev = 0
+    for T in (1, 2, 3, 17, 100, 1000, 10 ** 4, 10 ** 5, 10 ** 6):
+        p = rmsn.rmsn_plan(rmsn.OP_BWD, T, 2048, 1, 0, compensated=True)
+        assert p["workspace_bytes"] >= prev
+        assert p["grid"] <= min(T, SM * p["ctas_per_sm"])  # within the documented bound
+        prev = p["workspace_bytes"]
+
+
+def test_set_policy(lib):
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, threads=100)
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, warps_per_row=3)
+    try:
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, threads=512, ctas_per_sm=2, warps_per_row=4)
+        p = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
+        assert (p["threads"], p["ctas_per_sm"], p["warps_per_row"]) == (512, 2, 4)
+    finally:
+        rmsn.rmsn_set_policy(rmsn.OP_FWD)
+    p = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
+    assert (p["threads"], p["warps_per_row"]) == (256, 2)
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.randn(4, 64)
+    with pytest.raises(ValueError):
+        rmsn.rmsnorm_fwd(x, torch.ones(64))
+
+
+def test_product_never_imports_oracle():
+    """The product package does not import, load or name the oracle."""
+    pkg = os.path.join(ROOT, "rmsnorm_fwd_bwd_persistent_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "from oracle" not in src, fn
+                assert "liboracle" not in src and "rmsnorm_oracle" not in src, fn
