@@ -3,7 +3,7 @@ the RMSNorm hot path at T=8192, H=4096, bf16.
 
 One step = forward + deterministic fused backward (main strip kernel + dW column
 reduce) + fused residual-add/RMSNorm/E4M3 1x128 block quant, each on its own seeded
-synthetic inputs of the headline shape, with L2 flushed (a 512 MiB write) before every
+synthetic inputs of the headline shape, with L2 flushed (512 MiB written, 256 MiB read) before every
 op and each op timed with CUDA events on its stream (the pages' protocol: kernel time,
 cold L2, FlashInfer PR #5741 Performance; miles-ext-kernels PR #15 Performance).
 The bandwidth is the logical-byte model of the same pages divided by the step time.
@@ -184,7 +184,8 @@ class Step:
         self.scale = torch.empty(f.H // 128, wl.round_up(f.T, 4), device=dev)
         self.normed = torch.empty_like(self.fx)
         self.eps = c.eps
-        self.flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+        self.flush_buf = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+        self.flush_rd = self.flush_buf.view(torch.float32)[: (FLUSH_BYTES // 2) // 4]
         self.bytes = {
             "fwd": wl.fwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype),
             "bwd": wl.bwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype),
@@ -192,6 +193,12 @@ class Step:
         }
         # fwd writes rstd for the bwd once, so the bwd sees the forward's saved value
         rmsn.rmsnorm_fwd(self.x, self.w, self.eps, y=self.y, rstd=self.rstd)
+
+    def flush(self):
+        """Evicts L2: writes 512 MiB, then reads 256 MiB of it so that L2 holds clean lines
+        (no write-back of flush data lands inside the next timed op)."""
+        self.flush_buf.zero_()
+        self.flush_rd.sum()
 
     def fwd(self):
         self.rmsn.rmsnorm_fwd(self.x, self.w, self.eps, y=self.y, rstd=self.rstd)
@@ -217,7 +224,7 @@ def time_steps(step: Step, steps: int, warmup: int, world: int):
                for _ in range(steps)] for op in Step.OPS}
     for _ in range(warmup):
         for op in Step.OPS:
-            step.flush.zero_()
+            step.flush()
             step.run_op(op)
     torch.cuda.synchronize()
     _barrier(world)
@@ -225,7 +232,7 @@ def time_steps(step: Step, steps: int, warmup: int, world: int):
     t0 = time.perf_counter()
     for i in range(steps):
         for op in Step.OPS:
-            step.flush.zero_()  # L2 flush between timed ops (outside the events)
+            step.flush()  # L2 flush between timed ops (outside the events)
             s, e = ev[op][i]
             s.record()
             step.run_op(op)
@@ -415,7 +422,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; x, dy ~ N(0,1), residual ~ N(0,2), w = 1 + 0.1 N(0,1))",
         "config": {"workload": WORKLOAD, "T": T_MAIN, "H": H_MAIN, "x_dtype": "bf16",
                    "w_dtype": "bf16", "accumulate": "fp32", "bwd_mode": "deterministic",
-                   "l2": "flushed before every timed op (512 MiB write, outside the events)",
+                   "l2": "flushed before every timed op (512 MiB write + 256 MiB read, outside "
+                         "the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": {"bwd": "rmsnorm_bwd (main strip kernel + dW "

@@ -64,7 +64,8 @@ typedef enum {
     RMSN_ERR_UNSUPPORTED_SHAPE = 2,   /* H out of range or not a multiple of the vector */
     RMSN_ERR_MISALIGNED = 3,          /* a pointer violates its alignment */
     RMSN_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace smaller than rmsnorm_bwd_workspace_bytes */
-    RMSN_ERR_CUDA = 5                 /* a CUDA runtime call or a launch failed */
+    RMSN_ERR_CUDA = 5,                /* a CUDA runtime call or a launch failed */
+    RMSN_ERR_DEVICE_TIMEOUT = 6       /* rmsn_device_status: a kernel's bounded wait ran out */
 } rmsn_status;
 
 #define RMSN_MAX_H 16384
@@ -96,11 +97,12 @@ int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y,
  * Source: FlashInfer PR #5741, API (backward workspace query; caller-owned, reusable
  * across T) and Memory (per-chunk FP32 partials of dw).
  *
- * The workspace holds one FP32 partial row of dw per row chunk (two rows, high and low
- * part, when `compensated` is set).  The value returned for (T, H) is an upper bound
- * for every T' <= T with the same H, compensated flag and device, so one buffer can
- * be reused across calls.  `device` is a CUDA device ordinal (its SM count decides
- * the number of chunks).  Returns 0 for T <= 0, for an unsupported H, or when the
+ * The workspace holds, per row chunk, the chunk's dw partial as two FP32 rows (the
+ * high and low parts of a compensated sum): 8 * H bytes per chunk, at most
+ * (SM count x CTAs per SM) chunks and never more than T.  The value returned for (T, H)
+ * is an upper bound for every T' <= T with the same H and device, so one buffer can be
+ * reused across calls.  `device` is a CUDA device ordinal (its SM count decides the
+ * number of chunks); `compensated` does not change the size.  Returns 0 for T <= 0, for an unsupported H, or when the
  * device cannot be queried.
  * ---------------------------------------------------------------------------------- */
 size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int device);
@@ -122,18 +124,25 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *   rstd  [T] fp32 (device, read): the forward's saved rstd
  *   dx    [T, H] in x_dtype (device, written)
  *   dw    [H] fp32 (device, written, overwritten -- not accumulated into)
- *   deterministic  != 0: per-chunk partials go to the workspace and a second kernel
- *         folds them per column in a fixed order; dw is bitwise reproducible and a
- *         function of (T, H, dtypes, compensated, the device's SM count) only.
- *         == 0: dw is zeroed and the partials are added with FP32 atomics (no second
- *         kernel, no workspace; bits may differ from run to run).
- *   compensated  != 0: every dw partial is an FP32 (high, low) pair summed with the
- *         error-free TwoSum transformation, through the chunk fold and the column
- *         reduction; dw = high + low rounded once.
+ *   deterministic  != 0: each row chunk's partial goes to the workspace and a second
+ *         kernel sums the partials per column in a fixed order; dw is bitwise
+ *         reproducible and a function of (T, H, dtypes, compensated, the device's SM
+ *         count and shared memory, the launch policy) only.
+ *         == 0: dw is zeroed and the chunk partials are added to it with FP32 atomics
+ *         (no second kernel, no workspace; bits may differ from run to run, and the
+ *         cross-chunk sum is plain FP32, so above T ~ 65536 single elements can leave
+ *         the atol 1e-4 + rtol 1e-4 budget).
+ *   compensated  != 0: each thread adds every product dy*xhat to an FP32 (high, low)
+ *         pair with the error-free TwoSum transformation.
+ *         == 0: each thread sums the products of 4 consecutive rows with FMAs and adds
+ *         each such block sum to the (high, low) pair with TwoSum (blocked FP32 sums).
+ *         In both cases the chunk partials are (high, low) pairs and the column
+ *         reduction merges them with TwoSum; dw = high + low rounded once.
  *   workspace, workspace_bytes  device scratch of at least
  *         rmsnorm_bwd_workspace_bytes(T, H, compensated, device) bytes, 16-byte
  *         aligned; its contents on entry do not matter and on exit are unspecified.
  *         Needed when deterministic != 0; may be NULL / 0 otherwise.
+ *   x_dtype fp32 supports H <= 8192 (bf16: H <= RMSN_MAX_H).
  * Returns RMSN_OK or an error status (see conventions).
  * ---------------------------------------------------------------------------------- */
 int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w_dtype,
@@ -185,29 +194,48 @@ int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void*
  * ---------------------------------------------------------------------------------- */
 typedef enum { RMSN_OP_FWD = 0, RMSN_OP_BWD = 1, RMSN_OP_FUSED_QUANT = 2 } rmsn_op;
 
+/* Every kernel runs a persistent grid: a CTA is `consumer_warps` warps that share one
+ * row at a time plus one producer warp whose first lane streams the CTA's rows into a
+ * `stages`-deep shared-memory ring with bulk copies (cp.async.bulk, mbarrier-tracked).
+ * The forward and the fused quant give each CTA a contiguous block of rows; the
+ * backward's CTAs are its row chunks. */
 typedef struct {
     int vec_elems;        /* elements per 16-byte vector */
-    int warps_per_row;    /* warps that share one row */
-    int chunks_per_lane;  /* 16-byte vectors each lane holds per row (compile-time) */
-    int threads;          /* threads per CTA */
-    int rows_per_cta;     /* rows a CTA works on at once (threads / (32*warps_per_row)) */
-    int ctas_per_sm;      /* CTAs per SM the persistent grid is sized for */
+    int consumer_warps;   /* warps that share one row */
+    int chunks_per_lane;  /* 16-byte vectors each consumer lane holds per row */
+    int threads;          /* threads per CTA (consumer warps + one producer warp) */
+    int stages;           /* depth of the shared-memory row ring */
+    int ctas_per_sm;      /* CTAs per SM the grid is sized for */
     int64_t grid;         /* CTAs launched (for the backward: the number of row chunks) */
     int64_t smem_bytes;   /* dynamic shared memory per CTA */
     int64_t workspace_bytes; /* backward scratch (0 for the other ops) */
 } rmsn_plan_t;
 
-/* Fills *out for (op, T, H, dtypes, compensated) on a device with `sm_count` SMs.
+/* Fills *out for (op, T, H, dtypes) on a device with `sm_count` SMs and 228 KiB of
+ * shared memory per SM (sm_100 / sm_103).  `compensated` does not change the plan.
  * Returns RMSN_OK, or the status the corresponding entry point would return for an
  * unsupported shape or dtype. */
 int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compensated,
               int sm_count, rmsn_plan_t* out);
 
-/* Tuning hook for benchmarks: overrides the default threads per CTA, CTAs per SM and
- * warps per row of one op for the whole process (0 keeps a default).  Changing it while
+/* Tuning hook for benchmarks: overrides the consumer warps per CTA (a power of two
+ * <= 8), the CTAs per SM and the maximum ring depth of one op for the whole process
+ * (0 keeps a default).  The backward's chunk count, and so its dw bits, follow the CTAs
+ * per SM; rmsnorm_bwd_workspace_bytes reflects the current setting.  Changing it while
  * calls are in flight on other host threads is a race.  Returns RMSN_ERR_INVALID_ARG for
- * a combination the kernels cannot run (then nothing changes). */
-int rmsn_set_policy(int op, int threads, int ctas_per_sm, int warps_per_row);
+ * values out of range (then nothing changes). */
+int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages);
+
+/* ------------------------------------------------------------------------------------
+ * rmsn_device_status -- every wait inside the kernels (a consumer waiting for a row to
+ * land in shared memory, the producer waiting for a stage to be released) gives up after
+ * 1 s, sets a bit in a per-device error word and ends the kernel early instead of
+ * hanging; the outputs of that call are then incomplete.  This call synchronizes
+ * `stream`, reads and clears the current device's error word into *flags (bit 0: a row
+ * never landed; bit 1: a stage was never released; bit 2: copies were still in flight
+ * when a CTA gave up) and returns RMSN_OK if it was 0, RMSN_ERR_DEVICE_TIMEOUT otherwise.
+ * ---------------------------------------------------------------------------------- */
+int rmsn_device_status(rmsn_stream_t stream, unsigned* flags);
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,7 @@ __all__ = [
     "RMSN_F32", "RMSN_BF16", "RMSN_MAX_H", "RmsnError", "library_path", "load_library",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan", "rmsn_set_policy",
+    "rmsn_device_status",
     "OP_FWD", "OP_BWD", "OP_FUSED_QUANT",
 ]
 
@@ -42,9 +43,9 @@ class RmsnError(RuntimeError):
 
 
 class _Plan(ctypes.Structure):
-    _fields_ = [("vec_elems", ctypes.c_int), ("warps_per_row", ctypes.c_int),
+    _fields_ = [("vec_elems", ctypes.c_int), ("consumer_warps", ctypes.c_int),
                 ("chunks_per_lane", ctypes.c_int), ("threads", ctypes.c_int),
-                ("rows_per_cta", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("stages", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64)]
 
@@ -83,6 +84,8 @@ def load_library():
                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(_Plan)]
         L.rmsn_set_policy.restype = ctypes.c_int
         L.rmsn_set_policy.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.rmsn_device_status.restype = ctypes.c_int
+        L.rmsn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint)]
         _lib = L
         return _lib
 
@@ -242,6 +245,19 @@ def rmsn_plan(op: int, T: int, H: int, x_dtype: int, w_dtype: int, compensated: 
     return {f: getattr(p, f) for f, _ in _Plan._fields_}
 
 
-def rmsn_set_policy(op: int, threads: int = 0, ctas_per_sm: int = 0, warps_per_row: int = 0):
-    _check(load_library().rmsn_set_policy(int(op), int(threads), int(ctas_per_sm),
-                                          int(warps_per_row)), "rmsn_set_policy")
+def rmsn_set_policy(op: int, consumer_warps: int = 0, ctas_per_sm: int = 0, max_stages: int = 0):
+    _check(load_library().rmsn_set_policy(int(op), int(consumer_warps), int(ctas_per_sm),
+                                          int(max_stages)), "rmsn_set_policy")
+
+
+def rmsn_device_status(device: int | torch.device | None = None) -> int:
+    """Synchronizes the current stream and returns (and clears) the device error word:
+    0 if no kernel wait ran out since the last call."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    flags = ctypes.c_uint(0)
+    with torch.cuda.device(dev):
+        st = load_library().rmsn_device_status(
+            ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream), ctypes.byref(flags))
+    if st not in (0, 6):
+        _check(st, "rmsn_device_status")
+    return int(flags.value)

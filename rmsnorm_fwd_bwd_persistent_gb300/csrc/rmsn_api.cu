@@ -1,110 +1,121 @@
-// rmsn_api.cu -- the C ABI: argument checks, the launch planner, the per-device SM-count
-// cache and the exported entry points declared in include/rmsn.h.
+// rmsn_api.cu -- the C ABI: argument checks, the launch planner, the per-device property
+// cache, the device error word and the exported entry points declared in include/rmsn.h.
 //
 // Checks run before anything is enqueued and return a status (the validation of
 // FlashInfer PR #4480's wrapper: shape, dtype and alignment checked on the host, an
 // unsupported hidden size rejected instead of launched).  The planner is a pure host
-// function of (op, T, H, dtypes, flags, SM count), testable without a GPU
+// function of (op, T, H, dtypes, SM count, shared memory per SM), testable without a GPU
 // (Liger-Kernel PR #1336: fast-path eligibility helpers as pure functions).
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "rmsn.h"
 #include "rmsn_internal.h"
+#include "rmsn_pipe.cuh"
+
+// Device error word: bits set by kernels whose bounded waits ran out (rmsn_pipe.cuh).
+__device__ unsigned int g_rmsn_error_word;
 
 namespace {
 
 using rmsn::Launch;
 
+constexpr int64_t kDefaultSmemPerSm = 233472;   // 228 KiB on sm_100 / sm_103
+constexpr int64_t kDefaultSmemPerCta = 232448;  // 227 KiB opt-in maximum per CTA
+constexpr int64_t kSmemReservedPerCta = 1024;   // set aside by the driver for each CTA
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every pipeline wait gives up after 1 s
+
 // ------------------------------------------------------------------ policy defaults
 struct Policy {
-    int threads;
+    int consumer_warps;  // 0: derived from H (target_nch vectors per lane)
     int ctas_per_sm;
-    int wpr;        // 0: smallest count that fits the per-lane chunk budget
-    int max_nch;    // per-lane chunk budget (registers)
+    int max_stages;
+    int target_nch;
+    int max_nch;
 };
 
-// Defaults per op: FWD, BWD, FUSED.  Threads and CTAs per SM size the persistent grid;
-// the chunk budget bounds the per-lane register row cache.
+// Per op: FWD, BWD, FUSED.
 constexpr Policy kDefaultPolicy[3] = {
-    {256, 4, 0, 8},  // forward: row cache of up to 8 x 16 B per lane
-    {256, 2, 0, 4},  // backward: x and dy caches plus the dw accumulators
-    {256, 4, 0, 8},  // fused: x and residual caches
+    {0, 4, 3, 4, 16},  // forward: small CTAs, 4 per SM, a shallow ring
+    {0, 2, 3, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
+    {0, 4, 3, 4, 8},   // fused quant
 };
 Policy g_policy[3] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2]};
-std::mutex g_policy_mu;
+std::mutex g_mu;
 
-constexpr int kMaxDevices = 64;
-std::atomic<int> g_sm_count[kMaxDevices];
-
-int sm_count_of(int dev) {
-    if (dev < 0 || dev >= kMaxDevices) return 0;
-    int v = g_sm_count[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        return 0;
-    }
-    g_sm_count[dev].store(n, std::memory_order_relaxed);
-    return n;
+Policy policy(int op) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_policy[op];
 }
 
-int current_sm_count() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+// ------------------------------------------------------------------ device properties
+struct DevProps {
+    int sms = 0;
+    int64_t smem_sm = 0;
+    int64_t smem_cta = 0;
+    unsigned* err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DevProps g_props[kMaxDevices];
+std::atomic<bool> g_props_ready[kMaxDevices];
+
+const DevProps* props_of(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (g_props_ready[dev].load(std::memory_order_acquire)) return &g_props[dev];
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_props_ready[dev].load(std::memory_order_relaxed)) return &g_props[dev];
+    DevProps p;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
         cudaGetLastError();
-        return 0;
+        return nullptr;
     }
-    return sm_count_of(dev);
+    p.sms = v;
+    p.smem_sm = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+                        cudaSuccess ? v : kDefaultSmemPerSm;
+    p.smem_cta = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+                         cudaSuccess ? v : kDefaultSmemPerCta;
+    cudaGetLastError();
+    g_props[dev] = p;
+    g_props_ready[dev].store(true, std::memory_order_release);
+    return &g_props[dev];
+}
+
+// The error word's device address for the current device (needs its context current).
+unsigned* error_word(int dev) {
+    static std::atomic<unsigned*> addr[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned* p = addr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_rmsn_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    addr[dev].store(static_cast<unsigned*>(a), std::memory_order_release);
+    return static_cast<unsigned*>(a);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 int esize(int dt) { return dt == RMSN_F32 ? 4 : 2; }
-
 bool valid_dtype(int dt) { return dt == RMSN_F32 || dt == RMSN_BF16; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <size_t N>
-int pick_nch(const int (&set)[N], int need) {
+int pick_nch(const int (&set)[N], int64_t need) {
     for (size_t i = 0; i < N; ++i)
         if (set[i] >= need) return set[i];
     return 0;
 }
 
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// Chooses warps per row and the chunk variant: the smallest power-of-two warp count whose
-// per-lane chunk count fits the budget (so a row is read by as few lanes as possible, each
-// with a long run of 16-byte loads).
-int plan_geometry(int op, int64_t H, int vec, const Policy& P, Launch* L) {
-    const int64_t nvec = H / vec;
-    const int max_nch = P.max_nch;
-    int wpr = P.wpr;
-    if (wpr == 0) {
-        for (wpr = 1; wpr <= 16; wpr *= 2)
-            if (cdiv(nvec, 32 * wpr) <= max_nch) break;
-        if (wpr > 16) wpr = 16;  // over budget: the widest group, the largest compiled variant
-    }
-    const int need = (int)cdiv(nvec, 32 * wpr);
-    int nch = 0;
-    if (op == RMSN_OP_FWD) nch = pick_nch(rmsn::kFwdNch, need);
-    else if (op == RMSN_OP_BWD) nch = pick_nch(rmsn::kBwdNch, need);
-    else nch = pick_nch(rmsn::kFusedNch, need);
-    if (nch == 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
-    int threads = P.threads < 32 * wpr ? 32 * wpr : P.threads;
-    if (threads % (32 * wpr) != 0 || threads > 512) return RMSN_ERR_UNSUPPORTED_SHAPE;
-    const int groups = threads / (32 * wpr);
-    if (wpr > 1 && groups > 15) return RMSN_ERR_UNSUPPORTED_SHAPE;  // named barriers 1..15
-    L->wpr = wpr;
-    L->nch = nch;
-    L->threads = threads;
-    L->groups = groups;
-    return RMSN_OK;
-}
-
-int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int comp, int sms, Launch* L,
-         int64_t* ws_bytes) {
+// The launch plan of one call.  Consumer warps: the smallest power of two (<= 8) whose
+// lanes hold about `target_nch` 16-byte vectors of a row each; the chunk variant is the
+// smallest compiled count that covers the row.  Ring: as many stages (<= max_stages) as
+// the CTA's share of the SM's shared memory holds; fewer CTAs per SM if a share cannot
+// hold two stages.
+int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem_sm,
+         int64_t smem_cta, Launch* L, int64_t* ws_bytes) {
     if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
     if (!valid_dtype(x_dt) || !valid_dtype(w_dt)) return RMSN_ERR_INVALID_ARG;
     if (op == RMSN_OP_FUSED_QUANT && (x_dt != RMSN_BF16 || w_dt != RMSN_BF16))
@@ -113,85 +124,174 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int comp, int sms, La
     const int vec = 16 / esize(x_dt);
     if (H <= 0 || H > RMSN_MAX_H || H % vec != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
     if (op == RMSN_OP_FUSED_QUANT && H % 128 != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
-    Policy P;
-    {
-        std::lock_guard<std::mutex> lk(g_policy_mu);
-        P = g_policy[op];
+    const Policy P = policy(op);
+    const int64_t nvec = H / vec;
+    int nw = P.consumer_warps;
+    if (nw == 0) {
+        nw = 1;
+        while (nw < 8 && cdiv(nvec, 32 * nw) > P.target_nch) nw *= 2;
     }
-    int st = plan_geometry(op, H, vec, P, L);
-    if (st != RMSN_OK) return st;
-    const int64_t cap = (int64_t)sms * P.ctas_per_sm;
-    int64_t grid = cdiv(T, L->groups);
-    if (grid > cap) grid = cap;
+    const int64_t need = cdiv(nvec, 32 * nw);
+    int nch = 0;
+    if (op == RMSN_OP_FWD) nch = pick_nch(rmsn::kFwdNch, need);
+    else if (op == RMSN_OP_BWD) nch = pick_nch(rmsn::kBwdNch, need);
+    else nch = pick_nch(rmsn::kFusedNch, need);
+    if (nch == 0 || nch > P.max_nch) return RMSN_ERR_UNSUPPORTED_SHAPE;
+
+    const int64_t row_bytes = H * esize(x_dt);
+    const int64_t row_pad = cdiv(row_bytes, 128) * 128;
+    const int64_t stage_bytes = (op == RMSN_OP_FWD) ? row_pad : 2 * row_pad;
+    int cps = P.ctas_per_sm;
+    auto stages_for = [&](int c) -> int64_t {
+        int64_t share = smem_sm / c - kSmemReservedPerCta;
+        if (share > smem_cta) share = smem_cta;
+        return (share - rmsn::kRingHeader) / stage_bytes;
+    };
+    while (cps > 1 && stages_for(cps) < 2) --cps;
+    int64_t stages = stages_for(cps);
+    if (stages > P.max_stages) stages = P.max_stages;
+    if (stages < 1) return RMSN_ERR_UNSUPPORTED_SHAPE;
+
+    int64_t grid = (int64_t)sms * cps;
+    if (grid > T) grid = T;
     if (grid < 1) grid = 1;
+    L->nw = nw;
+    L->nch = nch;
+    L->stages = (int)stages;
+    L->ctas_per_sm = cps;
+    L->row_bytes = (uint32_t)row_bytes;
+    L->stage_bytes = (uint32_t)stage_bytes;
     L->grid = grid;
-    L->smem = 0;
-    if (ws_bytes) *ws_bytes = 0;
-    if (op == RMSN_OP_BWD) {
-        const int64_t parts = comp ? 2 : 1;
-        if (L->groups > 1) L->smem = H * 4 * parts;  // group fold buffer
-        if (ws_bytes) *ws_bytes = grid * H * 4 * parts;
-    }
+    L->smem = rmsn::kRingHeader + stages * stage_bytes;
+    L->err = nullptr;
+    L->limit_ns = kWaitLimitNs;
+    if (ws_bytes) *ws_bytes = (op == RMSN_OP_BWD) ? grid * H * 4 * 2 : 0;
     return RMSN_OK;
 }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA; }
 
+// Plans a call on the current device and fills in the device-dependent fields.
+int plan_current(int op, int64_t T, int64_t H, int x_dt, int w_dt, Launch* L, int64_t* ws) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSN_ERR_CUDA;
+    }
+    const DevProps* p = props_of(dev);
+    if (!p) return RMSN_ERR_CUDA;
+    int st = plan(op, T, H, x_dt, w_dt, p->sms, p->smem_sm, p->smem_cta, L, ws);
+    if (st != RMSN_OK) return st;
+    L->err = error_word(dev);
+    return L->err ? RMSN_OK : RMSN_ERR_CUDA;
+}
+
 }  // namespace
+
+namespace rmsn {
+
+cudaError_t allow_smem(const void* kernel, int64_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    struct Entry {
+        int dev;
+        const void* k;
+        int64_t bytes;
+    };
+    static std::vector<Entry> done;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& x : done)
+        if (x.dev == dev && x.k == kernel && x.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    for (auto& x : done)
+        if (x.dev == dev && x.k == kernel) {
+            x.bytes = bytes;
+            return cudaSuccess;
+        }
+    done.push_back({dev, kernel, bytes});
+    return cudaSuccess;
+}
+
+}  // namespace rmsn
 
 extern "C" {
 
 const char* rmsn_status_string(int status) {
     switch (status) {
         case RMSN_OK: return "ok";
-        case RMSN_ERR_INVALID_ARG: return "invalid argument (null pointer, dtype, T or eps)";
+        case RMSN_ERR_INVALID_ARG: return "invalid argument (null pointer, dtype, T, ld or eps)";
         case RMSN_ERR_UNSUPPORTED_SHAPE:
             return "unsupported shape (H must be a positive multiple of the 16-byte vector, "
-                   "at most 16384; the fused quant needs H % 128 == 0)";
+                   "at most 16384; the fused quant needs H % 128 == 0; the fp32 backward "
+                   "at most 8192)";
         case RMSN_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
         case RMSN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than rmsnorm_bwd_workspace_bytes";
         case RMSN_ERR_CUDA: return "CUDA error (launch or runtime call failed)";
+        case RMSN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out (device error word set)";
         default: return "unknown status";
     }
 }
 
 int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compensated,
               int sm_count, rmsn_plan_t* out) {
+    (void)compensated;
     if (!out) return RMSN_ERR_INVALID_ARG;
     Launch L{};
     int64_t ws = 0;
-    int st = plan(op, T, H, x_dtype, w_dtype, compensated, sm_count, &L, &ws);
+    int st = plan(op, T, H, x_dtype, w_dtype, sm_count, kDefaultSmemPerSm, kDefaultSmemPerCta,
+                  &L, &ws);
     if (st != RMSN_OK) return st;
-    Policy P;
-    {
-        std::lock_guard<std::mutex> lk(g_policy_mu);
-        P = g_policy[op];
-    }
     out->vec_elems = 16 / esize(x_dtype);
-    out->warps_per_row = L.wpr;
+    out->consumer_warps = L.nw;
     out->chunks_per_lane = L.nch;
-    out->threads = L.threads;
-    out->rows_per_cta = L.groups;
-    out->ctas_per_sm = P.ctas_per_sm;
+    out->threads = L.nw * 32 + 32;
+    out->stages = L.stages;
+    out->ctas_per_sm = L.ctas_per_sm;
     out->grid = L.grid;
     out->smem_bytes = L.smem;
     out->workspace_bytes = ws;
     return RMSN_OK;
 }
 
-int rmsn_set_policy(int op, int threads, int ctas_per_sm, int warps_per_row) {
+int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages) {
     if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
-    if (threads < 0 || threads > 512 || threads % 32 != 0) return RMSN_ERR_INVALID_ARG;
-    if (ctas_per_sm < 0 || ctas_per_sm > 32) return RMSN_ERR_INVALID_ARG;
-    if (warps_per_row < 0 || warps_per_row > 16 || (warps_per_row & (warps_per_row - 1)) != 0)
+    if (consumer_warps < 0 || consumer_warps > 8 ||
+        (consumer_warps & (consumer_warps - 1)) != 0)
         return RMSN_ERR_INVALID_ARG;
-    std::lock_guard<std::mutex> lk(g_policy_mu);
+    if (ctas_per_sm < 0 || ctas_per_sm > 16 || max_stages < 0 || max_stages > 32)
+        return RMSN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
     Policy p = kDefaultPolicy[op];
-    if (threads) p.threads = threads;
+    p.consumer_warps = consumer_warps;
     if (ctas_per_sm) p.ctas_per_sm = ctas_per_sm;
-    p.wpr = warps_per_row;
+    if (max_stages) p.max_stages = max_stages;
     g_policy[op] = p;
     return RMSN_OK;
+}
+
+int rmsn_device_status(rmsn_stream_t stream, unsigned* flags) {
+    if (!flags) return RMSN_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSN_ERR_CUDA;
+    }
+    unsigned* w = error_word(dev);
+    if (!w) return RMSN_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(w, 0, sizeof v) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSN_ERR_CUDA;
+    }
+    *flags = v;
+    return v ? RMSN_ERR_DEVICE_TIMEOUT : RMSN_OK;
 }
 
 int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y, float* rstd,
@@ -203,29 +303,23 @@ int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y,
     if (!x || !w || !y || !rstd) return RMSN_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(rstd, 4))
         return RMSN_ERR_MISALIGNED;
-    const int sms = current_sm_count();
-    if (sms <= 0) return RMSN_ERR_CUDA;
     Launch L{};
-    int st = plan(RMSN_OP_FWD, T, H, x_dtype, w_dtype, 0, sms, &L, nullptr);
+    int st = plan_current(RMSN_OP_FWD, T, H, x_dtype, w_dtype, &L, nullptr);
     if (st != RMSN_OK) return st;
     return from_cuda(rmsn::launch_fwd(L, x, x_dtype, w, w_dtype, y, rstd, T, H, eps,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int device) {
+    (void)compensated;
     if (T <= 0 || H <= 0 || H > RMSN_MAX_H || H % 4 != 0) return 0;
-    const int sms = sm_count_of(device);
-    if (sms <= 0) return 0;
-    Policy P;
-    {
-        std::lock_guard<std::mutex> lk(g_policy_mu);
-        P = g_policy[RMSN_OP_BWD];
-    }
+    const DevProps* p = props_of(device);
+    if (!p) return 0;
     // The chunk count never exceeds min(T, SMs * CTAs per SM) whatever the dtypes, and
     // grows with T, so this bounds every call with T' <= T.
-    int64_t chunks = (int64_t)sms * P.ctas_per_sm;
+    int64_t chunks = (int64_t)p->sms * policy(RMSN_OP_BWD).ctas_per_sm;
     if (chunks > T) chunks = T;
-    return (size_t)(chunks * H * 4 * (compensated ? 2 : 1));
+    return (size_t)(chunks * H * 4 * 2);
 }
 
 int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w_dtype,
@@ -241,17 +335,14 @@ int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w
     if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(w, 16) || !aligned(dx, 16) ||
         !aligned(rstd, 4))
         return RMSN_ERR_MISALIGNED;
-    const int sms = current_sm_count();
-    if (sms <= 0) return RMSN_ERR_CUDA;
+    if (deterministic && !workspace)
+        return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (deterministic && !aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
     Launch L{};
     int64_t need = 0;
-    int st = plan(RMSN_OP_BWD, T, H, x_dtype, w_dtype, compensated, sms, &L, &need);
+    int st = plan_current(RMSN_OP_BWD, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
-    if (deterministic) {
-        if (!workspace) return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
-        if (!aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
-        if ((int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
-    }
+    if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
     return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                       deterministic, compensated,
                                       static_cast<float*>(workspace), s));
@@ -268,10 +359,8 @@ int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void*
     if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(w, 16) || !aligned(normed, 16) ||
         !aligned(q, 16) || !aligned(block_scale, 4))
         return RMSN_ERR_MISALIGNED;
-    const int sms = current_sm_count();
-    if (sms <= 0) return RMSN_ERR_CUDA;
     Launch L{};
-    int st = plan(RMSN_OP_FUSED_QUANT, T, H, RMSN_BF16, RMSN_BF16, 0, sms, &L, nullptr);
+    int st = plan_current(RMSN_OP_FUSED_QUANT, T, H, RMSN_BF16, RMSN_BF16, &L, nullptr);
     if (st != RMSN_OK) return st;
     return from_cuda(rmsn::launch_fused(L, x, residual, w, q, block_scale, scale_ld, normed, T, H,
                                         eps, reinterpret_cast<cudaStream_t>(stream)));

@@ -1,28 +1,39 @@
 // rmsn_bwd.cu -- fused single-pass RMSNorm backward with a strip-reduced weight gradient.
 //
 // FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward: a persistent grid over
-// static row chunks; each CTA writes dx for its rows and keeps an FP32 dw partial for
-// its chunk; the partials are reduced per column in chunk order, with no atomics, so dw
-// depends only on (T, device).  Liger-Kernel PR #1336, Summary: the fused dX+dW
-// strip-reduction backward.  miles-ext-kernels PR #15, Changes: TwoSum per-thread
-// weight-gradient sums.
+// static row chunks; each CTA writes dx for its rows, dx = rstd*(g*w - mean(g*w*xhat)*xhat)
+// in FP32, and keeps an FP32 dw partial for its chunk (compensated summation); the
+// partials are reduced per column in a fixed order, so dw depends only on (T, device).
+// Liger-Kernel PR #1336, Summary: the fused dX+dW strip-reduction backward.
+// miles-ext-kernels PR #15, Changes: TwoSum per-thread weight-gradient sums (#8849) and
+// blocked FP32 weight-gradient sums (#8848).
 //
-// This build reduces the partials with a second kernel on the same stream (no grid-wide
-// barrier, so no CTA ever waits on another).
+// Main kernel: chunk c (= CTA c of a grid of n) owns the rows c, c + n, c + 2n, ...
+// (a static map, so the grid streams one window of consecutive rows at a time).  Its
+// producer thread streams the x and dy rows into a shared-memory ring; the consumer warps
+// take each row into registers, reduce sum((dy*w)*x) across the CTA, write dx from
+// registers, and add the row's dy*xhat into per-thread column accumulators that stay in
+// registers for the whole strip (each consumer thread owns the same columns for every
+// row; w stays in registers too).  The accumulators
+// carry a compensated (high, low) pair:
+//   compensated = 1: every product is added with TwoSum;
+//   compensated = 0: the products of kBlockRows consecutive rows are summed with FMAs and
+//                    each block sum is added with TwoSum ("blocked FP32 sums").
+// At the end of the strip the CTA writes its (high, low) partial row to the workspace
+// (deterministic mode) or adds high+low to dw with FP32 atomics.
 //
-// Main kernel, per CTA (chunk c owns rows [c*T/n, (c+1)*T/n)):
-//   each row group takes every `groups`-th row of the chunk; per row it loads x and dy
-//   into registers (16-byte vectors), forms xhat = x*rstd and g = dy*w, reduces
-//   sum(g*xhat) across the group, writes dx = rstd*(g - xhat*mean) and adds dy*xhat into
-//   per-lane column accumulators that live in registers for the whole strip.
-//   At the end the groups' accumulators are folded in group order through shared memory
-//   and the CTA writes one partial row (deterministic mode) or adds it to dw with FP32
-//   atomics (non-deterministic mode).
-// Column-reduce kernel: dw[j] = sum over chunks of partial[chunk][j], in a fixed order.
+// Column reduce kernel: dw[j] = sum over chunks of the (high, low) partials, in a fixed
+// order (contiguous chunk ranges summed in chunk order, then a fixed binary tree over the
+// ranges), every step a TwoSum merge, rounded once at the end.  It is launched as a
+// programmatic dependent of the main kernel so its launch overlaps the main kernel's tail;
+// it waits for the main kernel's memory before reading the partials.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
+#include "rmsn_pipe.cuh"
 
 namespace rmsn {
+
+constexpr int kBlockRows = 4;  // rows per FP32 block sum when compensated == 0
 
 struct BwdArgs {
     const void* dy;
@@ -32,254 +43,245 @@ struct BwdArgs {
     void* dx;
     float* dw;   // non-deterministic mode: zeroed dw, atomically accumulated
     float* ws;   // deterministic mode: [n_chunks, H] high parts, then [n_chunks, H] low parts
+    unsigned* err;
     int64_t T;
+    uint64_t limit_ns;
     int H;
-    int wpr;
+    int nw;
+    int stages;
+    uint32_t row_bytes;
+    uint32_t stage_bytes;
     int atomic;
 };
 
 template <typename TX, typename TW, int NCH, bool COMP>
-__global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
-    constexpr int NL = COMP ? NCH : 1;  // low-part accumulators (unused when !COMP)
-    extern __shared__ float fold[];     // [H] running high parts (+ [H] low parts)
-    __shared__ float red[2 * 32];
-    const int G = 32 * a.wpr;
-    const int groups = blockDim.x / G;
-    const int group = threadIdx.x / G;
-    const int gl = threadIdx.x - group * G;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const Ring ring = ring_at(smem, a.stages, a.stage_bytes);
+    const int nw = a.nw;
+    const int64_t nch = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t nrows = (a.T - 1 - b) / nch + 1;  // rows b, b + n, ... below T
+    const uint32_t dy_off = a.stage_bytes / 2;  // stage = [x row | dy row], each padded
+    ring_init(ring, nw);
+
+    if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
+        if ((threadIdx.x & 31) == 0) {
+            const uint8_t* X = static_cast<const uint8_t*>(a.x);
+            const uint8_t* DY = static_cast<const uint8_t*>(a.dy);
+            const int64_t issued = ring_produce(
+                ring, nrows, a.limit_ns, a.err, [&](int64_t k, uint8_t* dst, uint64_t* full) {
+                    const int64_t off = (b + k * nch) * (int64_t)a.row_bytes;
+                    mbar_arrive_expect_tx(full, 2 * a.row_bytes);
+                    bulk_load(dst, X + off, a.row_bytes, full);
+                    bulk_load(dst + dy_off, DY + off, a.row_bytes, full);
+                });
+            ring_drain(ring, issued, a.limit_ns, a.err);
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    const int NC = nw * 32;
     const int H = a.H;
     const int nvec = H / VEC;
     const float Hf = (float)H;
-    const int64_t nch = gridDim.x;
-    const int64_t r0 = (int64_t)blockIdx.x * a.T / nch;
-    const int64_t r1 = ((int64_t)blockIdx.x + 1) * a.T / nch;
-
-    const TX* __restrict__ DY = static_cast<const TX*>(a.dy);
-    const TX* __restrict__ X = static_cast<const TX*>(a.x);
-    const TW* __restrict__ W = static_cast<const TW*>(a.w);
     TX* __restrict__ DX = static_cast<TX*>(a.dx);
+    WReg<TW, VEC> wr[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int v = c * NC + t;
+        if (v < nvec) wr[c].load(static_cast<const TW*>(a.w), (int64_t)v * VEC);
+    }
 
-    float acc[NCH][VEC];
-    float accl[NL][VEC];
+    constexpr int NB = COMP ? 1 : NCH;  // block-sum registers (blocked mode only)
+    float hi[NCH][VEC], lo[NCH][VEC], blk[NB][VEC];
 #pragma unroll
     for (int c = 0; c < NCH; ++c)
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) acc[c][k] = 0.f;
+        for (int q = 0; q < VEC; ++q) hi[c][q] = lo[c][q] = 0.f;
 #pragma unroll
-    for (int c = 0; c < NL; ++c)
+    for (int c = 0; c < NB; ++c)
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) accl[c][k] = 0.f;
+        for (int q = 0; q < VEC; ++q) blk[c][q] = 0.f;
 
-    int parity = 0;
-    for (int64_t row = r0 + group; row < r1; row += groups) {
-        const int64_t base = row * H;
+    int64_t k = 0;
+    for (; k < nrows; ++k) {
+        const int64_t row = b + k * nch;
+        const float rs = __ldg(a.rstd + row);
+        const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
+        const uint8_t* st = ring.stage((int)(k % ring.stages));
         uint4 xv[NCH], dv[NCH];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int v = c * G + gl;
-            const bool ok = v < nvec;
-            xv[c] = ok ? ld_stream(X + base + (int64_t)v * VEC) : make_uint4(0, 0, 0, 0);
-            dv[c] = ok ? ld_stream(DY + base + (int64_t)v * VEC) : make_uint4(0, 0, 0, 0);
+            const int v = c * NC + t;
+            const bool in = ok && v < nvec;
+            xv[c] = in ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+            dv[c] = in ? lds128(st + dy_off + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
         }
-        const float rs = __ldg(a.rstd + row);
+        if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
 
+        // sum_j (dy_j * w_j) * x_j over the row
         float dot = 0.f;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int v = c * G + gl;
+            const int v = c * NC + t;
             if (v < nvec) {
                 float xf[VEC], df[VEC], wf[VEC];
                 Elem<TX>::unpack(xv[c], xf);
                 Elem<TX>::unpack(dv[c], df);
-                load_w<TW, VEC>(W, (int64_t)v * VEC, wf);
+                wr[c].get(wf);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const float xh = __fmul_rn(xf[k], rs);
-                    const float g = __fmul_rn(df[k], wf[k]);
-                    dot = fmaf(g, xh, dot);
-                }
+                for (int q = 0; q < VEC; ++q) dot = fmaf(__fmul_rn(df[q], wf[q]), xf[q], dot);
             }
         }
-        dot = group_sum(dot, a.wpr, red, group, parity);
-        parity ^= 1;
-        const float cm = __fdiv_rn(dot, Hf);
+        if (!consumer_sum(smem, dot, ok, nw, (int)(k & 1))) break;
+        // c = mean_j(g_j * xhat_j) = rstd * sum_j(g_j * x_j) / H
+        const float cm = __fdiv_rn(__fmul_rn(rs, dot), Hf);
 
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int v = c * G + gl;
+            const int v = c * NC + t;
             if (v < nvec) {
                 float xf[VEC], df[VEC], wf[VEC], o[VEC];
                 Elem<TX>::unpack(xv[c], xf);
                 Elem<TX>::unpack(dv[c], df);
-                load_w<TW, VEC>(W, (int64_t)v * VEC, wf);
+                wr[c].get(wf);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const float xh = __fmul_rn(xf[k], rs);
-                    const float g = __fmul_rn(df[k], wf[k]);
-                    o[k] = __fmul_rn(rs, fmaf(-xh, cm, g));
-                    const float p = __fmul_rn(df[k], xh);
+                for (int q = 0; q < VEC; ++q) {
+                    const float xh = __fmul_rn(xf[q], rs);
+                    const float g = __fmul_rn(df[q], wf[q]);
+                    o[q] = __fmul_rn(rs, fmaf(-xh, cm, g));
                     if constexpr (COMP) {
-                        comp_add(acc[c][k], accl[c][k], p);
+                        comp_add(hi[c][q], lo[c][q], __fmul_rn(df[q], xh));
                     } else {
-                        acc[c][k] = __fadd_rn(acc[c][k], p);
+                        blk[c][q] = fmaf(df[q], xh, blk[c][q]);
                     }
                 }
-                st_stream(DX + base + (int64_t)v * VEC, Elem<TX>::pack(o));
+                st_stream(DX + row * H + (int64_t)v * VEC, Elem<TX>::pack(o));
             }
+        }
+        if constexpr (!COMP) {
+            if ((k + 1) % kBlockRows == 0) {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) {
+                        comp_add(hi[c][q], lo[c][q], blk[c][q]);
+                        blk[c][q] = 0.f;
+                    }
+            }
+        }
+    }
+    if (k < nrows) return;  // gave up (error word set): leave the outputs as they are
+    if constexpr (!COMP) {
+        if (nrows % kBlockRows != 0) {
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) comp_add(hi[c][q], lo[c][q], blk[c][q]);
         }
     }
 
-    // ---- fold the row groups' partials in group order, then emit the chunk's partial
-    for (int gi = 0; gi < groups; ++gi) {
-        if (group == gi) {
+    // ---- emit the chunk's partial
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                const int v = c * G + gl;
-                if (v < nvec) {
-                    const int col0 = v * VEC;
-                    float hv[VEC], lv[VEC];
+    for (int c = 0; c < NCH; ++c) {
+        const int v = c * NC + t;
+        if (v < nvec) {
+            const int col0 = v * VEC;
+            if (a.atomic) {
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) {
-                        float h = acc[c][k];
-                        float l = COMP ? accl[COMP ? c : 0][k] : 0.f;
-                        if (gi > 0) {
-                            if constexpr (COMP) {
-                                float fh = fold[col0 + k], fl = fold[H + col0 + k];
-                                comp_merge(fh, fl, h, l);
-                                h = fh;
-                                l = fl;
-                            } else {
-                                h = __fadd_rn(fold[col0 + k], h);
-                            }
-                        }
-                        hv[k] = h;
-                        lv[k] = l;
-                    }
-                    if (gi + 1 < groups) {
+                for (int q = 0; q < VEC; ++q) atomicAdd(a.dw + col0 + q, __fadd_rn(hi[c][q], lo[c][q]));
+            } else {
+                float* dh = a.ws + (int64_t)blockIdx.x * H + col0;
+                float* dl = dh + nch * H;
 #pragma unroll
-                        for (int k = 0; k < VEC; ++k) {
-                            fold[col0 + k] = hv[k];
-                            if constexpr (COMP) fold[H + col0 + k] = lv[k];
-                        }
-                    } else if (a.atomic) {
-#pragma unroll
-                        for (int k = 0; k < VEC; ++k)
-                            atomicAdd(a.dw + col0 + k, COMP ? __fadd_rn(hv[k], lv[k]) : hv[k]);
-                    } else {
-                        float* dst = a.ws + (int64_t)blockIdx.x * H + col0;
-#pragma unroll
-                        for (int k = 0; k < VEC; k += 4)
-                            *reinterpret_cast<float4*>(dst + k) =
-                                make_float4(hv[k], hv[k + 1], hv[k + 2], hv[k + 3]);
-                        if constexpr (COMP) {
-                            float* dl = dst + nch * H;
-#pragma unroll
-                            for (int k = 0; k < VEC; k += 4)
-                                *reinterpret_cast<float4*>(dl + k) =
-                                    make_float4(lv[k], lv[k + 1], lv[k + 2], lv[k + 3]);
-                        }
-                    }
+                for (int q = 0; q < VEC; q += 4) {
+                    *reinterpret_cast<float4*>(dh + q) =
+                        make_float4(hi[c][q], hi[c][q + 1], hi[c][q + 2], hi[c][q + 3]);
+                    *reinterpret_cast<float4*>(dl + q) =
+                        make_float4(lo[c][q], lo[c][q + 1], lo[c][q + 2], lo[c][q + 3]);
                 }
             }
         }
-        if (groups > 1) __syncthreads();
     }
+    // Let the column-reduce grid start launching; it still waits for this grid's memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// dw[j] = sum_{chunk} ws[chunk][j] in a fixed order: the 8 warps of a CTA each add a
-// contiguous range of chunks in chunk order, and warp 0 adds the 8 range sums in range
-// order.  One CTA covers 128 columns (a float4 per lane).
-template <bool COMP>
+// dw[j] = fixed-order compensated sum over the chunk partials.  A CTA covers 16 columns
+// (4 lanes x float4); its 256 threads form 64 splits, split s adds the chunks
+// [s*n/64, (s+1)*n/64) in chunk order; the 64 split sums are merged by a fixed binary tree.
+constexpr int kSplits = 64;
+
 __global__ void __launch_bounds__(256) rmsnorm_dw_reduce_kernel(const float* __restrict__ ws,
                                                                 float* __restrict__ dw, int H,
-                                                                int n_chunks) {
-    __shared__ float4 part[8][32];
-    __shared__ float4 partl[8][32];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int col = (blockIdx.x * 32 + lane) * 4;
+                                                                int n) {
+    __shared__ float4 ph[kSplits][4];
+    __shared__ float4 pl[kSplits][4];
+    const int cl = threadIdx.x & 3;
+    const int sp = threadIdx.x >> 2;
+    const int col = (blockIdx.x * 4 + cl) * 4;
     const bool ok = col < H;
-    const int k0 = warp * n_chunks / 8;
-    const int k1 = (warp + 1) * n_chunks / 8;
-    const int64_t lo_off = (int64_t)n_chunks * H;
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+    const int k0 = (int)((int64_t)sp * n / kSplits);
+    const int k1 = (int)((int64_t)(sp + 1) * n / kSplits);
+    const int64_t lo_off = (int64_t)n * H;
+
+    // wait for the main kernel's partials (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
-        int k = k0;
-        for (; k + 4 <= k1; k += 4) {
-            float4 v[4], vl[4];
+        for (int k = k0; k < k1; k += 4) {
+            float4 vh[4], vl[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                v[u] = __ldcg(reinterpret_cast<const float4*>(ws + (int64_t)(k + u) * H + col));
-                if constexpr (COMP)
-                    vl[u] = __ldcg(reinterpret_cast<const float4*>(ws + lo_off +
-                                                                   (int64_t)(k + u) * H + col));
+                if (k + u < k1) {
+                    vh[u] = __ldcg(reinterpret_cast<const float4*>(ws + (int64_t)(k + u) * H + col));
+                    vl[u] = __ldcg(reinterpret_cast<const float4*>(ws + lo_off + (int64_t)(k + u) * H + col));
+                }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float hv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                if constexpr (COMP) {
-                    const float lv[4] = {vl[u].x, vl[u].y, vl[u].z, vl[u].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) comp_merge(s[q], e[q], hv[q], lv[q]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) s[q] = __fadd_rn(s[q], hv[q]);
+                if (k + u < k1) {
+                    comp_merge(sh[0], sl[0], vh[u].x, vl[u].x);
+                    comp_merge(sh[1], sl[1], vh[u].y, vl[u].y);
+                    comp_merge(sh[2], sl[2], vh[u].z, vl[u].z);
+                    comp_merge(sh[3], sl[3], vh[u].w, vl[u].w);
                 }
             }
         }
-        for (; k < k1; ++k) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(ws + (int64_t)k * H + col));
-            const float hv[4] = {v.x, v.y, v.z, v.w};
-            if constexpr (COMP) {
-                const float4 vl =
-                    __ldcg(reinterpret_cast<const float4*>(ws + lo_off + (int64_t)k * H + col));
-                const float lv[4] = {vl.x, vl.y, vl.z, vl.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) comp_merge(s[q], e[q], hv[q], lv[q]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) s[q] = __fadd_rn(s[q], hv[q]);
-            }
-        }
     }
-    part[warp][lane] = make_float4(s[0], s[1], s[2], s[3]);
-    if constexpr (COMP) partl[warp][lane] = make_float4(e[0], e[1], e[2], e[3]);
+    ph[sp][cl] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+    pl[sp][cl] = make_float4(sl[0], sl[1], sl[2], sl[3]);
     __syncthreads();
-    if (warp == 0 && ok) {
-        float t[4] = {s[0], s[1], s[2], s[3]}, te[4] = {e[0], e[1], e[2], e[3]};
-        for (int w = 1; w < 8; ++w) {
-            const float4 p = part[w][lane];
-            const float ph[4] = {p.x, p.y, p.z, p.w};
-            if constexpr (COMP) {
-                const float4 pl = partl[w][lane];
-                const float pv[4] = {pl.x, pl.y, pl.z, pl.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) comp_merge(t[q], te[q], ph[q], pv[q]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) t[q] = __fadd_rn(t[q], ph[q]);
-            }
+    for (int half = kSplits / 2; half >= 1; half >>= 1) {
+        if (sp < half) {
+            const float4 bh = ph[sp + half][cl], bl = pl[sp + half][cl];
+            float4 ah = ph[sp][cl], al = pl[sp][cl];
+            comp_merge(ah.x, al.x, bh.x, bl.x);
+            comp_merge(ah.y, al.y, bh.y, bl.y);
+            comp_merge(ah.z, al.z, bh.z, bl.z);
+            comp_merge(ah.w, al.w, bh.w, bl.w);
+            ph[sp][cl] = ah;
+            pl[sp][cl] = al;
         }
-        float4 out;
-        if constexpr (COMP)
-            out = make_float4(__fadd_rn(t[0], te[0]), __fadd_rn(t[1], te[1]),
-                              __fadd_rn(t[2], te[2]), __fadd_rn(t[3], te[3]));
-        else
-            out = make_float4(t[0], t[1], t[2], t[3]);
-        *reinterpret_cast<float4*>(dw + col) = out;
+        __syncthreads();
+    }
+    if (sp == 0 && ok) {
+        const float4 h = ph[0][cl], l = pl[0][cl];
+        *reinterpret_cast<float4*>(dw + col) = make_float4(
+            __fadd_rn(h.x, l.x), __fadd_rn(h.y, l.y), __fadd_rn(h.z, l.z), __fadd_rn(h.w, l.w));
     }
 }
 
 template <typename TX, typename TW, int NCH, bool COMP>
 static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s) {
     auto k = rmsnorm_bwd_kernel<TX, TW, NCH, COMP>;
-    if (L.smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)L.smem);
-        if (e != cudaSuccess) return e;
-    }
-    k<<<(unsigned)L.grid, L.threads, (size_t)L.smem, s>>>(a);
+    cudaError_t e = allow_smem((const void*)k, L.smem);
+    if (e != cudaSuccess) return e;
+    k<<<(unsigned)L.grid, L.nw * 32 + 32, (size_t)L.smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -304,7 +306,8 @@ static cudaError_t dispatch_comp(const Launch& L, const BwdArgs& a, int comp, cu
 cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt, const void* w,
                        int w_dt, const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
                        int deterministic, int compensated, float* ws, cudaStream_t s) {
-    BwdArgs a{dy, x, w, rstd, dx, dw, ws, T, (int)H, L.wpr, deterministic ? 0 : 1};
+    BwdArgs a{dy, x, w, rstd, dx, dw, ws, L.err, T, L.limit_ns, (int)H, L.nw, L.stages,
+              L.row_bytes, L.stage_bytes, deterministic ? 0 : 1};
     if (!deterministic) {
         cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s);
         if (e != cudaSuccess) return e;
@@ -316,12 +319,19 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
     else if (x_dt == 0 && w_dt == 1) e = dispatch_comp<float, __nv_bfloat16>(L, a, compensated, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess || !deterministic) return e;
-    const unsigned rgrid = (unsigned)((H + 127) / 128);
-    if (compensated)
-        rmsnorm_dw_reduce_kernel<true><<<rgrid, 256, 0, s>>>(ws, dw, (int)H, (int)L.grid);
-    else
-        rmsnorm_dw_reduce_kernel<false><<<rgrid, 256, 0, s>>>(ws, dw, (int)H, (int)L.grid);
-    return cudaGetLastError();
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((H + 15) / 16));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_dw_reduce_kernel, (const float*)ws, dw, (int)H,
+                              (int)L.grid);
 }
 
 }  // namespace rmsn

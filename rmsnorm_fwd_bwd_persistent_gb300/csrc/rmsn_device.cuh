@@ -1,10 +1,10 @@
-// rmsn_device.cuh -- device helpers shared by the RMSNorm kernels (sm_103a).
+// rmsn_device.cuh -- element conversions, register-resident weights and compensated sums
+// shared by the RMSNorm kernels (sm_103a).
 //
-// Row geometry used by every kernel: a "row group" of G = 32 * wpr consecutive threads
-// owns one row at a time.  The row is split into 16-byte vectors; lane l of the group
-// holds vectors v = c * G + l for c = 0 .. NCH-1 (NCH is a compile-time count, vectors
-// past the end of the row are masked), so one warp-wide access touches 512 contiguous
-// bytes and every load is a coalesced 16-byte access.
+// Row geometry used by every kernel: the NC consumer threads of a CTA share one row at a
+// time.  The row is split into 16-byte vectors; consumer thread t holds the vectors
+// v = c * NC + t for c = 0 .. NCH-1 (NCH is a compile-time count, vectors past the end of
+// the row are masked), so one warp-wide access touches 512 contiguous bytes.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -58,74 +58,57 @@ struct Elem<__nv_bfloat16> {
 };
 
 // ------------------------------------------------------------------ memory access
-// Streamed operands (read or written once per call): evict-first cache policy.
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
-}
+// Streamed outputs (written once per call): evict-first cache policy.
 __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
-// The weight is re-read by every row: read-only path, default (L1-resident) policy.
-// Loads the VEC weights that sit beside a 16-byte vector of x (VEC = 16 / sizeof(x)).
+// The weights a lane needs for one 16-byte vector of x, kept packed in registers for the
+// whole life of a persistent CTA (every row uses the same columns of w).
 template <typename TW, int VEC>
-__device__ __forceinline__ void load_w(const TW* w, int64_t col0, float (&f)[VEC]);
+struct WReg;
 
 template <>
-__device__ __forceinline__ void load_w<float, 4>(const float* w, int64_t col0, float (&f)[4]) {
-    float4 a = __ldg(reinterpret_cast<const float4*>(w + col0));
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-}
+struct WReg<__nv_bfloat16, 8> {
+    uint4 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* w, int64_t col0) {
+        v = __ldg(reinterpret_cast<const uint4*>(w + col0));
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const { Elem<__nv_bfloat16>::unpack(v, f); }
+};
 template <>
-__device__ __forceinline__ void load_w<float, 8>(const float* w, int64_t col0, float (&f)[8]) {
-    float4 a = __ldg(reinterpret_cast<const float4*>(w + col0));
-    float4 b = __ldg(reinterpret_cast<const float4*>(w + col0 + 4));
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
+struct WReg<__nv_bfloat16, 4> {
+    uint2 v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* w, int64_t col0) {
+        v = __ldg(reinterpret_cast<const uint2*>(w + col0));
+    }
+    __device__ __forceinline__ void get(float (&f)[4]) const {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    }
+};
 template <>
-__device__ __forceinline__ void load_w<__nv_bfloat16, 8>(const __nv_bfloat16* w, int64_t col0,
-                                                         float (&f)[8]) {
-    uint4 a = __ldg(reinterpret_cast<const uint4*>(w + col0));
-    Elem<__nv_bfloat16>::unpack(a, f);
-}
+struct WReg<float, 8> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* w, int64_t col0) {
+        a = __ldg(reinterpret_cast<const float4*>(w + col0));
+        b = __ldg(reinterpret_cast<const float4*>(w + col0 + 4));
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const {
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+};
 template <>
-__device__ __forceinline__ void load_w<__nv_bfloat16, 4>(const __nv_bfloat16* w, int64_t col0,
-                                                         float (&f)[4]) {
-    uint2 a = __ldg(reinterpret_cast<const uint2*>(w + col0));
-    f[0] = bf16_lo(a.x); f[1] = bf16_hi(a.x);
-    f[2] = bf16_lo(a.y); f[3] = bf16_hi(a.y);
-}
-
-// ------------------------------------------------------------------ reductions
-// Butterfly sum over a warp.  IEEE addition is commutative, so every lane ends with the
-// same bits.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__device__ __forceinline__ void named_barrier(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Sum over the wpr warps of one row group.  `red` is a shared array of 2 * (CTA warps)
-// floats; `parity` alternates per row so that a warp that moves on to the next row never
-// overwrites a slot another warp of its group has not read yet.  Groups synchronize on
-// their own named barrier (id 1 + group), never on the CTA barrier.  The warp sums are
-// added in warp order, so the result is the same on every lane of the group.
-__device__ __forceinline__ float group_sum(float v, int wpr, float* red, int group, int parity) {
-    v = warp_sum(v);
-    if (wpr == 1) return v;
-    const int warp = threadIdx.x >> 5;
-    float* slot = red + parity * (blockDim.x >> 5) + group * wpr;
-    if ((threadIdx.x & 31) == 0) red[parity * (blockDim.x >> 5) + warp] = v;
-    named_barrier(1 + group, 32 * wpr);
-    float s = slot[0];
-    for (int k = 1; k < wpr; ++k) s += slot[k];
-    return s;
-}
+struct WReg<float, 4> {
+    float4 a;
+    __device__ __forceinline__ void load(const float* w, int64_t col0) {
+        a = __ldg(reinterpret_cast<const float4*>(w + col0));
+    }
+    __device__ __forceinline__ void get(float (&f)[4]) const {
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    }
+};
 
 // ------------------------------------------------------------------ compensated sums
 // Error-free transformation of a + b (Knuth's TwoSum): s + e == a + b exactly.

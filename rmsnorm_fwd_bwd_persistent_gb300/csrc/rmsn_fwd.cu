@@ -2,11 +2,16 @@
 // Design/Forward: FP32 sum of squares, two-level shuffle/shared reduce, IEEE rsqrt in
 // FP32, one pass that writes y and the FP32 rstd).
 //
-// A persistent grid walks the rows with a grid stride; each row group (one or more
-// warps, Liger-Kernel PR #1336 review: "each warp handles separate tokens") keeps its
-// row in registers between the reduction and the write, so x is read from HBM once.
+// CTA b takes the rows b, b + G, b + 2G, ... (G = grid size), so at any moment the whole
+// grid streams one window of consecutive rows.  Its producer thread streams those rows
+// into a shared-memory ring with bulk copies; the consumer warps take a row out of the
+// ring into registers (16-byte vectors, lane-contiguous so every warp access is 512
+// contiguous bytes), release the stage, reduce sum(x^2) across the consumer warps, and
+// write y straight from registers; w stays in registers for the CTA's lifetime.  x is
+// read from HBM exactly once.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
+#include "rmsn_pipe.cuh"
 
 namespace rmsn {
 
@@ -15,90 +20,120 @@ struct FwdArgs {
     const void* w;
     void* y;
     float* rstd;
+    unsigned* err;
     int64_t T;
+    uint64_t limit_ns;
     int H;
-    int wpr;
+    int nw;
+    int stages;
+    uint32_t row_bytes;
+    uint32_t stage_bytes;
     float eps;
 };
 
 template <typename TX, typename TW, int NCH>
-__global__ void __launch_bounds__(512) rmsnorm_fwd_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
-    __shared__ float red[2 * 32];
-    const int G = 32 * a.wpr;
-    const int groups = blockDim.x / G;
-    const int group = threadIdx.x / G;
-    const int gl = threadIdx.x - group * G;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const Ring ring = ring_at(smem, a.stages, a.stage_bytes);
+    const int nw = a.nw;
+    const int64_t G = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t nrows = (a.T - 1 - b) / G + 1;  // rows b, b + G, ... below T
+    ring_init(ring, nw);
+
+    if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
+        if ((threadIdx.x & 31) == 0) {
+            const uint8_t* X = static_cast<const uint8_t*>(a.x);
+            const int64_t issued = ring_produce(
+                ring, nrows, a.limit_ns, a.err, [&](int64_t k, uint8_t* dst, uint64_t* full) {
+                    mbar_arrive_expect_tx(full, a.row_bytes);
+                    bulk_load(dst, X + (b + k * G) * (int64_t)a.row_bytes, a.row_bytes, full);
+                });
+            ring_drain(ring, issued, a.limit_ns, a.err);
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    const int NC = nw * 32;
     const int nvec = a.H / VEC;
     const float Hf = (float)a.H;
-    const TX* __restrict__ X = static_cast<const TX*>(a.x);
-    const TW* __restrict__ W = static_cast<const TW*>(a.w);
     TX* __restrict__ Y = static_cast<TX*>(a.y);
+    WReg<TW, VEC> wr[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int v = c * NC + t;
+        if (v < nvec) wr[c].load(static_cast<const TW*>(a.w), (int64_t)v * VEC);
+    }
 
-    int parity = 0;
-    for (int64_t row = (int64_t)blockIdx.x * groups + group; row < a.T;
-         row += (int64_t)gridDim.x * groups) {
-        const TX* xr = X + row * a.H;
+    for (int64_t k = 0; k < nrows; ++k) {
+        const int64_t row = b + k * G;
+        const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
+        const uint8_t* st = ring.stage((int)(k % ring.stages));
         uint4 xv[NCH];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int v = c * G + gl;
-            xv[c] = (v < nvec) ? ld_stream(xr + (int64_t)v * VEC) : make_uint4(0, 0, 0, 0);
+            const int v = c * NC + t;
+            xv[c] = (ok && v < nvec) ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
         }
+        if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
+
         float ss = 0.f;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             float f[VEC];
             Elem<TX>::unpack(xv[c], f);
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) ss = fmaf(f[k], f[k], ss);
+            for (int q = 0; q < VEC; ++q) ss = fmaf(f[q], f[q], ss);
         }
-        ss = group_sum(ss, a.wpr, red, group, parity);
-        parity ^= 1;
-        const float ms = __fdiv_rn(ss, Hf);
-        const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, a.eps)));
-        if (gl == 0) a.rstd[row] = rs;
+        if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
+        const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
+        if (t == 0) a.rstd[row] = rs;
 
         TX* yr = Y + row * a.H;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int v = c * G + gl;
+            const int v = c * NC + t;
             if (v < nvec) {
                 float f[VEC], wf[VEC];
                 Elem<TX>::unpack(xv[c], f);
-                load_w<TW, VEC>(W, (int64_t)v * VEC, wf);
+                wr[c].get(wf);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) f[k] = __fmul_rn(__fmul_rn(f[k], rs), wf[k]);
+                for (int q = 0; q < VEC; ++q) f[q] = __fmul_rn(__fmul_rn(f[q], rs), wf[q]);
                 st_stream(yr + (int64_t)v * VEC, Elem<TX>::pack(f));
             }
         }
     }
 }
 
+template <typename TX, typename TW, int NCH>
+static cudaError_t run(const Launch& L, const FwdArgs& a, cudaStream_t s) {
+    auto k = rmsnorm_fwd_kernel<TX, TW, NCH>;
+    cudaError_t e = allow_smem((const void*)k, L.smem);
+    if (e != cudaSuccess) return e;
+    k<<<(unsigned)L.grid, L.nw * 32 + 32, (size_t)L.smem, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename TX, typename TW>
 static cudaError_t dispatch(const Launch& L, const FwdArgs& a, cudaStream_t s) {
-#define RMSN_FWD_CASE(N)                                                                  \
-    case N:                                                                               \
-        rmsnorm_fwd_kernel<TX, TW, N><<<(unsigned)L.grid, L.threads, 0, s>>>(a);          \
-        return cudaGetLastError();
     switch (L.nch) {
-        RMSN_FWD_CASE(1)
-        RMSN_FWD_CASE(2)
-        RMSN_FWD_CASE(3)
-        RMSN_FWD_CASE(4)
-        RMSN_FWD_CASE(5)
-        RMSN_FWD_CASE(6)
-        RMSN_FWD_CASE(8)
-        RMSN_FWD_CASE(12)
-        default:
-            return cudaErrorInvalidConfiguration;
+        case 1: return run<TX, TW, 1>(L, a, s);
+        case 2: return run<TX, TW, 2>(L, a, s);
+        case 3: return run<TX, TW, 3>(L, a, s);
+        case 4: return run<TX, TW, 4>(L, a, s);
+        case 6: return run<TX, TW, 6>(L, a, s);
+        case 8: return run<TX, TW, 8>(L, a, s);
+        case 16: return run<TX, TW, 16>(L, a, s);
+        default: return cudaErrorInvalidConfiguration;
     }
-#undef RMSN_FWD_CASE
 }
 
 cudaError_t launch_fwd(const Launch& L, const void* x, int x_dt, const void* w, int w_dt,
                        void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s) {
-    FwdArgs a{x, w, y, rstd, T, (int)H, L.wpr, eps};
+    FwdArgs a{x, w, y, rstd, L.err, T, L.limit_ns, (int)H, L.nw, L.stages, L.row_bytes,
+              L.stage_bytes, eps};
     if (x_dt == 1 && w_dt == 1) return dispatch<__nv_bfloat16, __nv_bfloat16>(L, a, s);
     if (x_dt == 1 && w_dt == 0) return dispatch<__nv_bfloat16, float>(L, a, s);
     if (x_dt == 0 && w_dt == 0) return dispatch<float, float>(L, a, s);

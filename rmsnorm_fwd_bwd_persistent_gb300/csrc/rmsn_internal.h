@@ -7,17 +7,23 @@
 namespace rmsn {
 
 // Geometry of one launch (chosen by the planner in rmsn_api.cu).
+//   Each CTA = `nw` consumer warps that share one row at a time + 1 producer warp whose
+//   lane 0 streams the CTA's rows into a `stages`-deep shared-memory ring.
 struct Launch {
-    int wpr;        // warps per row group
-    int nch;        // 16-byte vectors per lane per row (compile-time variant)
-    int threads;    // threads per CTA
-    int groups;     // row groups per CTA = threads / (32 * wpr)
-    int64_t grid;   // CTAs (backward: row chunks)
-    int64_t smem;   // dynamic shared memory bytes
+    int nw;              // consumer warps per CTA
+    int nch;             // 16-byte vectors per consumer lane per row (compile-time variant)
+    int stages;          // ring depth
+    int ctas_per_sm;     // CTAs per SM the grid is sized for
+    uint32_t row_bytes;  // bytes of one input row
+    uint32_t stage_bytes;// bytes of one stage (one or two padded rows)
+    int64_t grid;        // CTAs (backward: row chunks)
+    int64_t smem;        // dynamic shared memory bytes per CTA
+    unsigned* err;       // device error word (bounded waits that ran out)
+    uint64_t limit_ns;   // time limit of every wait
 };
 
 // Chunk counts with a compiled kernel variant, per op (ascending).
-constexpr int kFwdNch[] = {1, 2, 3, 4, 5, 6, 8, 12};
+constexpr int kFwdNch[] = {1, 2, 3, 4, 6, 8, 16};
 constexpr int kBwdNch[] = {1, 2, 3, 4, 6, 8};
 constexpr int kFusedNch[] = {1, 2, 3, 4, 6, 8};
 
@@ -32,5 +38,8 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
 cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const void* w,
                          uint8_t* q, float* block_scale, int64_t scale_ld, void* normed,
                          int64_t T, int64_t H, float eps, cudaStream_t s);
+
+// Opt a kernel into more than 48 KiB of dynamic shared memory (once per kernel).
+cudaError_t allow_smem(const void* kernel, int64_t bytes);
 
 }  // namespace rmsn

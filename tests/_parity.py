@@ -72,6 +72,7 @@ def check_fwd(x: torch.Tensor, w: torch.Tensor, eps: float) -> dict:
     else:
         out["y"] = gates.check_f32_rel(y_dev, y_ref)
     out["guards"] = {"n_fail": int(not (guards_ok(ybuf) and guards_ok(rbuf)))}
+    out["device_status"] = {"n_fail": rmsn.rmsn_device_status()}
     out["_rstd_dev"] = rstd
     return out
 
@@ -105,6 +106,7 @@ def check_bwd(dy, x, w, rstd, deterministic=True, compensated=False, full_dw=Tru
         _, dw_ref = oracle.rmsnorm_bwd(wl.to_oracle(dy), wl.to_oracle(x), W, r_all, want_dx=False)
         out["dw"] = gates.check_dw(dw.cpu().numpy(), dw_ref)
     out["guards"] = {"n_fail": int(not (guards_ok(dxbuf) and guards_ok(dwbuf)))}
+    out["device_status"] = {"n_fail": rmsn.rmsn_device_status()}
     out["_dw_dev"] = dw
     return out
 
@@ -134,6 +136,7 @@ def check_fused(x, res, w, eps, ld_pad: int = 0) -> dict:
         # pad entries m in [T, ld) keep the poison (NaN) the test wrote
         "scale_pads": {"n_fail": int(np.count_nonzero(~np.isnan(s_dev[~valid])))},
         "guards": {"n_fail": int(not (guards_ok(qbuf) and guards_ok(sbuf) and guards_ok(nbuf)))},
+        "device_status": {"n_fail": rmsn.rmsn_device_status()},
     }
     return out
 

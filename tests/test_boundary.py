@@ -36,14 +36,14 @@ def test_exports_every_declared_function(lib):
     names = _declared_functions()
     assert {"rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
             "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan",
-            "rmsn_set_policy"} <= set(names)
+            "rmsn_set_policy", "rmsn_device_status"} <= set(names)
     raw = ctypes.CDLL(rmsn.library_path())
     for n in names:
         assert hasattr(raw, n), f"{n} declared in rmsn.h but not exported"
 
 
 def test_status_strings(lib):
-    for s in range(0, 6):
+    for s in range(0, 7):
         assert rmsn.rmsn_status_string(s) and rmsn.rmsn_status_string(s) != "unknown status"
     assert rmsn.rmsn_status_string(99) == "unknown status"
 
@@ -103,27 +103,36 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         with pytest.raises(rmsn.RmsnError):
             rmsn.rmsn_plan(op, 100, H, xd, wd)
         return
+    if op == rmsn.OP_BWD and xd == 0 and H > 8192:
+        with pytest.raises(rmsn.RmsnError):
+            rmsn.rmsn_plan(op, 100, H, xd, wd)
+        return
     for T in (1, 65, 8192, 262144):
         p = rmsn.rmsn_plan(op, T, H, xd, wd, sm_count=SM)
-        lanes = 32 * p["warps_per_row"]
+        lanes = 32 * p["consumer_warps"]
         assert p["vec_elems"] == vec
         assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
-        assert p["threads"] % lanes == 0 and p["threads"] <= 512
-        assert p["rows_per_cta"] == p["threads"] // lanes
-        assert 1 <= p["grid"] <= SM * p["ctas_per_sm"]
-        assert p["grid"] <= -(-T // p["rows_per_cta"])              # no idle CTAs
+        assert p["threads"] == lanes + 32 and p["threads"] <= 288   # + one producer warp
+        assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
+        row = H * (2 if xd == 1 else 4)
+        stage = -(-row // 128) * 128 * (1 if op == rmsn.OP_FWD else 2)
+        assert p["stages"] >= 1 and p["smem_bytes"] == 1024 + p["stages"] * stage
+        assert p["ctas_per_sm"] * (p["smem_bytes"] + 1024) <= 233472  # fits the SM
+        if p["ctas_per_sm"] > 1:
+            assert p["stages"] >= 2
         if op == rmsn.OP_FUSED_QUANT:
             assert lanes % 16 == 0                                  # 16 lanes hold one block
 
 
 def test_plan_headline_geometry(lib):
     f = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
-    assert (f["warps_per_row"], f["chunks_per_lane"]) == (2, 8)
+    assert (f["consumer_warps"], f["chunks_per_lane"], f["ctas_per_sm"], f["stages"]) == (4, 4, 4, 3)
     b = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1)
-    assert (b["warps_per_row"], b["chunks_per_lane"]) == (4, 4)
-    assert b["workspace_bytes"] == b["grid"] * 4096 * 4
-    bc = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1, compensated=True)
-    assert bc["workspace_bytes"] == 2 * bc["grid"] * 4096 * 4
+    assert (b["consumer_warps"], b["chunks_per_lane"], b["ctas_per_sm"]) == (8, 2, 2)
+    assert b["grid"] == 2 * SM
+    assert b["workspace_bytes"] == 2 * b["grid"] * 4096 * 4       # (high, low) rows per chunk
+    q = rmsn.rmsn_plan(rmsn.OP_FUSED_QUANT, 8192, 4096, 1, 1)
+    assert (q["consumer_warps"], q["chunks_per_lane"]) == (4, 4)
 
 
 def test_workspace_grows_with_t(lib):
@@ -137,17 +146,19 @@ def test_workspace_grows_with_t(lib):
 
 def test_set_policy(lib):
     with pytest.raises(rmsn.RmsnError):
-        rmsn.rmsn_set_policy(rmsn.OP_FWD, threads=100)
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, consumer_warps=3)
     with pytest.raises(rmsn.RmsnError):
-        rmsn.rmsn_set_policy(rmsn.OP_FWD, warps_per_row=3)
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, consumer_warps=16)
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, max_stages=33)
     try:
-        rmsn.rmsn_set_policy(rmsn.OP_FWD, threads=512, ctas_per_sm=2, warps_per_row=4)
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, consumer_warps=8, ctas_per_sm=2, max_stages=3)
         p = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
-        assert (p["threads"], p["ctas_per_sm"], p["warps_per_row"]) == (512, 2, 4)
+        assert (p["threads"], p["ctas_per_sm"], p["stages"]) == (288, 2, 3)
     finally:
         rmsn.rmsn_set_policy(rmsn.OP_FWD)
     p = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
-    assert (p["threads"], p["warps_per_row"]) == (256, 2)
+    assert (p["threads"], p["consumer_warps"]) == (160, 4)
 
 
 def test_binding_rejects_cpu_tensors(lib):

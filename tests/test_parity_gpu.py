@@ -91,6 +91,10 @@ def test_bwd_parity_shapes(T, H, xd, wd, mode):
         pytest.skip("H not a multiple of the vector")
     x, dy, w = wl.fwd_bwd_inputs(_wl(wl.MAIN_BF16, T, H, xd, wd), DEV, seed=T * 7 + H)
     _, rstd = rmsn.rmsnorm_fwd(x, w, 1e-6)
+    if xd == torch.float32 and H > 8192:  # the fp32 backward supports H <= 8192
+        with pytest.raises(rmsn.RmsnError):
+            rmsn.rmsnorm_bwd(dy, x, w, rstd)
+        return
     r = P.check_bwd(dy, x, w, rstd, deterministic=mode.startswith("det"),
                     compensated=mode.endswith("comp"))
     P.assert_ok(r, f"bwd T={T} H={H} {xd}/{wd} {mode}")
