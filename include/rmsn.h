@@ -126,8 +126,8 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *   dw    [H] fp32 (device, written, overwritten -- not accumulated into)
  *   deterministic  != 0: each row chunk's partial goes to the workspace and a second
  *         kernel sums the partials per column in a fixed order; dw is bitwise
- *         reproducible and a function of (T, H, dtypes, compensated, the device's SM
- *         count and shared memory, the launch policy) only.
+ *         reproducible and a function of (T, H, dtypes, compensated, the device, the
+ *         library build and the launch policy) only.
  *         == 0: dw is zeroed and the chunk partials are added to it with FP32 atomics
  *         (no second kernel, no workspace; bits may differ from run to run, and the
  *         cross-chunk sum is plain FP32, so above T ~ 65536 single elements can leave
@@ -196,9 +196,11 @@ typedef enum { RMSN_OP_FWD = 0, RMSN_OP_BWD = 1, RMSN_OP_FUSED_QUANT = 2 } rmsn_
 
 /* Every kernel runs a persistent grid: a CTA is `consumer_warps` warps that share one
  * row at a time plus one producer warp whose first lane streams the CTA's rows into a
- * `stages`-deep shared-memory ring with bulk copies (cp.async.bulk, mbarrier-tracked).
- * The forward and the fused quant give each CTA a contiguous block of rows; the
- * backward's CTAs are its row chunks. */
+ * `stages`-deep shared-memory ring with bulk copies (cp.async.bulk, mbarrier-tracked);
+ * the weight vector is copied to shared memory once per CTA.  CTA b of a grid of G takes
+ * the rows b, b + G, b + 2G, ...; the backward's CTAs are its row chunks.  At launch the
+ * grid is clamped to the CTAs that are resident at once (the kernel's occupancy), so
+ * `grid` below is an upper bound. */
 typedef struct {
     int vec_elems;        /* elements per 16-byte vector */
     int consumer_warps;   /* warps that share one row */

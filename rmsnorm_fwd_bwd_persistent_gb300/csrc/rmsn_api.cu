@@ -111,9 +111,10 @@ int pick_nch(const int (&set)[N], int64_t need) {
 
 // The launch plan of one call.  Consumer warps: the smallest power of two (<= 8) whose
 // lanes hold about `target_nch` 16-byte vectors of a row each; the chunk variant is the
-// smallest compiled count that covers the row.  Ring: as many stages (<= max_stages) as
-// the CTA's share of the SM's shared memory holds; fewer CTAs per SM if a share cannot
-// hold two stages.
+// smallest compiled count that covers the row.  Shared memory per CTA: the ring header,
+// the weight vector, and as many stages (<= max_stages) as the CTA's share of the SM
+// holds; fewer CTAs per SM if a share cannot hold two stages.  The grid is clamped again
+// at launch to what is resident at once (fit_grid).
 int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem_sm,
          int64_t smem_cta, Launch* L, int64_t* ws_bytes) {
     if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
@@ -141,11 +142,13 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     const int64_t row_bytes = H * esize(x_dt);
     const int64_t row_pad = cdiv(row_bytes, 128) * 128;
     const int64_t stage_bytes = (op == RMSN_OP_FWD) ? row_pad : 2 * row_pad;
+    const int64_t w_bytes = H * esize(w_dt);
+    const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
     int cps = P.ctas_per_sm;
     auto stages_for = [&](int c) -> int64_t {
         int64_t share = smem_sm / c - kSmemReservedPerCta;
         if (share > smem_cta) share = smem_cta;
-        return (share - rmsn::kRingHeader) / stage_bytes;
+        return (share - data_off) / stage_bytes;
     };
     while (cps > 1 && stages_for(cps) < 2) --cps;
     int64_t stages = stages_for(cps);
@@ -159,10 +162,13 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     L->nch = nch;
     L->stages = (int)stages;
     L->ctas_per_sm = cps;
+    L->sms = sms;
     L->row_bytes = (uint32_t)row_bytes;
     L->stage_bytes = (uint32_t)stage_bytes;
+    L->w_bytes = (uint32_t)w_bytes;
+    L->data_off = (uint32_t)data_off;
     L->grid = grid;
-    L->smem = rmsn::kRingHeader + stages * stage_bytes;
+    L->smem = data_off + stages * stage_bytes;
     L->err = nullptr;
     L->limit_ns = kWaitLimitNs;
     if (ws_bytes) *ws_bytes = (op == RMSN_OP_BWD) ? grid * H * 4 * 2 : 0;
@@ -190,29 +196,53 @@ int plan_current(int op, int64_t T, int64_t H, int x_dt, int w_dt, Launch* L, in
 
 namespace rmsn {
 
-cudaError_t allow_smem(const void* kernel, int64_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+cudaError_t fit_grid(const void* kernel, const Launch& L, int threads, int64_t* grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    struct Entry {
+    const DevProps* p = props_of(dev);
+    if (!p) return cudaErrorInvalidDevice;
+    // The dynamic shared memory limit is a per-kernel attribute: it is raised once to the
+    // device's opt-in maximum (a limit, not a reservation), never lowered, so any plan's
+    // size launches.  Occupancy is cached per (kernel, threads, shared memory).
+    struct Occ {
         int dev;
         const void* k;
-        int64_t bytes;
+        int threads;
+        int64_t smem;
+        int occ;
     };
-    static std::vector<Entry> done;
+    struct Opted {
+        int dev;
+        const void* k;
+    };
+    static std::vector<Occ> occs;
+    static std::vector<Opted> opted;
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
-    for (auto& x : done)
-        if (x.dev == dev && x.k == kernel && x.bytes >= bytes) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    for (auto& x : done)
-        if (x.dev == dev && x.k == kernel) {
-            x.bytes = bytes;
-            return cudaSuccess;
+    int occ = 0;
+    for (const auto& x : occs)
+        if (x.dev == dev && x.k == kernel && x.threads == threads && x.smem == L.smem) {
+            occ = x.occ;
+            break;
         }
-    done.push_back({dev, kernel, bytes});
+    if (occ == 0) {
+        bool done = false;
+        for (const auto& x : opted)
+            if (x.dev == dev && x.k == kernel) done = true;
+        if (!done) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)p->smem_cta);
+            if (e != cudaSuccess) return e;
+            opted.push_back({dev, kernel});
+        }
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, (size_t)L.smem);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        occs.push_back({dev, kernel, threads, L.smem, occ});
+    }
+    const int64_t resident = (int64_t)L.sms * occ;
+    *grid = L.grid < resident ? L.grid : resident;
     return cudaSuccess;
 }
 

@@ -11,10 +11,11 @@
 // Main kernel: chunk c (= CTA c of a grid of n) owns the rows c, c + n, c + 2n, ...
 // (a static map, so the grid streams one window of consecutive rows at a time).  Its
 // producer thread streams the x and dy rows into a shared-memory ring; the consumer warps
-// take each row into registers, reduce sum((dy*w)*x) across the CTA, write dx from
-// registers, and add the row's dy*xhat into per-thread column accumulators that stay in
-// registers for the whole strip (each consumer thread owns the same columns for every
-// row; w stays in registers too).  The accumulators
+// read each row from its stage twice -- once to reduce sum((dy*w)*x) across the CTA,
+// once to write dx and add the row's dy*xhat into per-thread column accumulators that
+// stay in registers for the whole strip -- and then release the stage.  Each consumer
+// thread owns the same columns for every row; w is copied to shared memory once per CTA,
+// so the registers hold little besides the accumulators.  The accumulators
 // carry a compensated (high, low) pair:
 //   compensated = 1: every product is added with TwoSum;
 //   compensated = 0: the products of kBlockRows consecutive rows are summed with FMAs and
@@ -51,6 +52,8 @@ struct BwdArgs {
     int stages;
     uint32_t row_bytes;
     uint32_t stage_bytes;
+    uint32_t w_bytes;
+    uint32_t data_off;
     int atomic;
 };
 
@@ -58,12 +61,14 @@ template <typename TX, typename TW, int NCH, bool COMP>
 __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
-    const Ring ring = ring_at(smem, a.stages, a.stage_bytes);
+    const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);
+    const uint8_t* wsm = smem + kRingHeader;
     const int nw = a.nw;
     const int64_t nch = gridDim.x;
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / nch + 1;  // rows b, b + n, ... below T
     const uint32_t dy_off = a.stage_bytes / 2;  // stage = [x row | dy row], each padded
+    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -88,12 +93,6 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     const int nvec = H / VEC;
     const float Hf = (float)H;
     TX* __restrict__ DX = static_cast<TX*>(a.dx);
-    WReg<TW, VEC> wr[NCH];
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int v = c * NC + t;
-        if (v < nvec) wr[c].load(static_cast<const TW*>(a.w), (int64_t)v * VEC);
-    }
 
     constexpr int NB = COMP ? 1 : NCH;  // block-sum registers (blocked mode only)
     float hi[NCH][VEC], lo[NCH][VEC], blk[NB][VEC];
@@ -112,26 +111,17 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
         const float rs = __ldg(a.rstd + row);
         const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
         const uint8_t* st = ring.stage((int)(k % ring.stages));
-        uint4 xv[NCH], dv[NCH];
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int v = c * NC + t;
-            const bool in = ok && v < nvec;
-            xv[c] = in ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-            dv[c] = in ? lds128(st + dy_off + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-        }
-        if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
 
-        // sum_j (dy_j * w_j) * x_j over the row
+        // pass 1: sum_j (dy_j * w_j) * x_j over the row (x, dy read from the stage)
         float dot = 0.f;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
-            if (v < nvec) {
+            if (ok && v < nvec) {
                 float xf[VEC], df[VEC], wf[VEC];
-                Elem<TX>::unpack(xv[c], xf);
-                Elem<TX>::unpack(dv[c], df);
-                wr[c].get(wf);
+                Elem<TX>::unpack(lds128(st + (size_t)v * 16), xf);
+                Elem<TX>::unpack(lds128(st + dy_off + (size_t)v * 16), df);
+                WSmem<TW, VEC>::get(wsm, v, wf);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) dot = fmaf(__fmul_rn(df[q], wf[q]), xf[q], dot);
             }
@@ -140,14 +130,15 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
         // c = mean_j(g_j * xhat_j) = rstd * sum_j(g_j * x_j) / H
         const float cm = __fdiv_rn(__fmul_rn(rs, dot), Hf);
 
+        // pass 2: dx and the dw accumulators (x, dy read from the stage again)
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (v < nvec) {
                 float xf[VEC], df[VEC], wf[VEC], o[VEC];
-                Elem<TX>::unpack(xv[c], xf);
-                Elem<TX>::unpack(dv[c], df);
-                wr[c].get(wf);
+                Elem<TX>::unpack(lds128(st + (size_t)v * 16), xf);
+                Elem<TX>::unpack(lds128(st + dy_off + (size_t)v * 16), df);
+                WSmem<TW, VEC>::get(wsm, v, wf);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) {
                     const float xh = __fmul_rn(xf[q], rs);
@@ -162,6 +153,7 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
                 st_stream(DX + row * H + (int64_t)v * VEC, Elem<TX>::pack(o));
             }
         }
+        ring_release(ring, k);  // every consumer warp has read the stage twice
         if constexpr (!COMP) {
             if ((k + 1) % kBlockRows == 0) {
 #pragma unroll
@@ -276,47 +268,51 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce_kernel(const float* __r
     }
 }
 
+// Launches the main kernel; *grid receives the number of chunks it ran with.
 template <typename TX, typename TW, int NCH, bool COMP>
-static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s) {
+static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s, int64_t* grid) {
     auto k = rmsnorm_bwd_kernel<TX, TW, NCH, COMP>;
-    cudaError_t e = allow_smem((const void*)k, L.smem);
+    const int threads = L.nw * 32 + 32;
+    cudaError_t e = fit_grid((const void*)k, L, threads, grid);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)L.grid, L.nw * 32 + 32, (size_t)L.smem, s>>>(a);
+    k<<<(unsigned)*grid, threads, (size_t)L.smem, s>>>(a);
     return cudaGetLastError();
 }
 
 template <typename TX, typename TW, bool COMP>
-static cudaError_t dispatch_nch(const Launch& L, const BwdArgs& a, cudaStream_t s) {
+static cudaError_t dispatch_nch(const Launch& L, const BwdArgs& a, cudaStream_t s, int64_t* g) {
     switch (L.nch) {
-        case 1: return run_main<TX, TW, 1, COMP>(L, a, s);
-        case 2: return run_main<TX, TW, 2, COMP>(L, a, s);
-        case 3: return run_main<TX, TW, 3, COMP>(L, a, s);
-        case 4: return run_main<TX, TW, 4, COMP>(L, a, s);
-        case 6: return run_main<TX, TW, 6, COMP>(L, a, s);
-        case 8: return run_main<TX, TW, 8, COMP>(L, a, s);
+        case 1: return run_main<TX, TW, 1, COMP>(L, a, s, g);
+        case 2: return run_main<TX, TW, 2, COMP>(L, a, s, g);
+        case 3: return run_main<TX, TW, 3, COMP>(L, a, s, g);
+        case 4: return run_main<TX, TW, 4, COMP>(L, a, s, g);
+        case 6: return run_main<TX, TW, 6, COMP>(L, a, s, g);
+        case 8: return run_main<TX, TW, 8, COMP>(L, a, s, g);
         default: return cudaErrorInvalidConfiguration;
     }
 }
 
 template <typename TX, typename TW>
-static cudaError_t dispatch_comp(const Launch& L, const BwdArgs& a, int comp, cudaStream_t s) {
-    return comp ? dispatch_nch<TX, TW, true>(L, a, s) : dispatch_nch<TX, TW, false>(L, a, s);
+static cudaError_t dispatch_comp(const Launch& L, const BwdArgs& a, int comp, cudaStream_t s,
+                                 int64_t* g) {
+    return comp ? dispatch_nch<TX, TW, true>(L, a, s, g) : dispatch_nch<TX, TW, false>(L, a, s, g);
 }
 
 cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt, const void* w,
                        int w_dt, const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
                        int deterministic, int compensated, float* ws, cudaStream_t s) {
     BwdArgs a{dy, x, w, rstd, dx, dw, ws, L.err, T, L.limit_ns, (int)H, L.nw, L.stages,
-              L.row_bytes, L.stage_bytes, deterministic ? 0 : 1};
+              L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off, deterministic ? 0 : 1};
     if (!deterministic) {
         cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e;
-    if (x_dt == 1 && w_dt == 1) e = dispatch_comp<__nv_bfloat16, __nv_bfloat16>(L, a, compensated, s);
-    else if (x_dt == 1 && w_dt == 0) e = dispatch_comp<__nv_bfloat16, float>(L, a, compensated, s);
-    else if (x_dt == 0 && w_dt == 0) e = dispatch_comp<float, float>(L, a, compensated, s);
-    else if (x_dt == 0 && w_dt == 1) e = dispatch_comp<float, __nv_bfloat16>(L, a, compensated, s);
+    int64_t g = 0;  // chunks the main kernel ran with
+    if (x_dt == 1 && w_dt == 1) e = dispatch_comp<__nv_bfloat16, __nv_bfloat16>(L, a, compensated, s, &g);
+    else if (x_dt == 1 && w_dt == 0) e = dispatch_comp<__nv_bfloat16, float>(L, a, compensated, s, &g);
+    else if (x_dt == 0 && w_dt == 0) e = dispatch_comp<float, float>(L, a, compensated, s, &g);
+    else if (x_dt == 0 && w_dt == 1) e = dispatch_comp<float, __nv_bfloat16>(L, a, compensated, s, &g);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess || !deterministic) return e;
 
@@ -331,7 +327,7 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, rmsnorm_dw_reduce_kernel, (const float*)ws, dw, (int)H,
-                              (int)L.grid);
+                              (int)g);
 }
 
 }  // namespace rmsn

@@ -63,50 +63,50 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
-// The weights a lane needs for one 16-byte vector of x, kept packed in registers for the
-// whole life of a persistent CTA (every row uses the same columns of w).
+// The weights beside one 16-byte vector v of x, read from the copy of w in shared memory
+// (VEC = 16 / sizeof(x) weights of type TW, at byte offset v * VEC * sizeof(TW)).
 template <typename TW, int VEC>
-struct WReg;
+struct WSmem;
 
 template <>
-struct WReg<__nv_bfloat16, 8> {
-    uint4 v;
-    __device__ __forceinline__ void load(const __nv_bfloat16* w, int64_t col0) {
-        v = __ldg(reinterpret_cast<const uint4*>(w + col0));
-    }
-    __device__ __forceinline__ void get(float (&f)[8]) const { Elem<__nv_bfloat16>::unpack(v, f); }
-};
-template <>
-struct WReg<__nv_bfloat16, 4> {
-    uint2 v;
-    __device__ __forceinline__ void load(const __nv_bfloat16* w, int64_t col0) {
-        v = __ldg(reinterpret_cast<const uint2*>(w + col0));
-    }
-    __device__ __forceinline__ void get(float (&f)[4]) const {
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-        f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+struct WSmem<__nv_bfloat16, 8> {
+    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[8]) {
+        uint4 u;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 16)));
+        Elem<__nv_bfloat16>::unpack(u, f);
     }
 };
 template <>
-struct WReg<float, 8> {
-    float4 a, b;
-    __device__ __forceinline__ void load(const float* w, int64_t col0) {
-        a = __ldg(reinterpret_cast<const float4*>(w + col0));
-        b = __ldg(reinterpret_cast<const float4*>(w + col0 + 4));
-    }
-    __device__ __forceinline__ void get(float (&f)[8]) const {
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+struct WSmem<__nv_bfloat16, 4> {
+    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[4]) {
+        uint32_t a, b;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(a), "=r"(b)
+                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 8)));
+        f[0] = bf16_lo(a); f[1] = bf16_hi(a);
+        f[2] = bf16_lo(b); f[3] = bf16_hi(b);
     }
 };
 template <>
-struct WReg<float, 4> {
-    float4 a;
-    __device__ __forceinline__ void load(const float* w, int64_t col0) {
-        a = __ldg(reinterpret_cast<const float4*>(w + col0));
+struct WSmem<float, 8> {
+    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[8]) {
+        const uint32_t addr = (uint32_t)__cvta_generic_to_shared(w + (size_t)v * 32);
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+                     : "r"(addr));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+                     : "r"(addr + 16));
     }
-    __device__ __forceinline__ void get(float (&f)[4]) const {
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+};
+template <>
+struct WSmem<float, 4> {
+    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[4]) {
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 16)));
     }
 };
 

@@ -16,8 +16,8 @@
 //
 // The page's kernel runs one CTA per row in a single wave; here the grid is persistent:
 // CTA b streams the rows b, b + G, ... (x and residual) through a shared-memory ring
-// filled by bulk copies, and its consumer warps share one row at a time; w stays in
-// registers.
+// filled by bulk copies, and its consumer warps share one row at a time; w is copied to
+// shared memory once per CTA.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
@@ -40,6 +40,8 @@ struct FusedArgs {
     int stages;
     uint32_t row_bytes;
     uint32_t stage_bytes;
+    uint32_t w_bytes;
+    uint32_t data_off;
     float eps;
 };
 
@@ -49,15 +51,17 @@ __device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
 }
 
 template <int NCH>
-__global__ void __launch_bounds__(288, 2) fused_add_rmsnorm_fp8_kernel(FusedArgs a) {
+__global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs a) {
     constexpr int VEC = 8;
     extern __shared__ __align__(128) uint8_t smem[];
-    const Ring ring = ring_at(smem, a.stages, a.stage_bytes);
+    const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);
+    const uint8_t* wsm = smem + kRingHeader;
     const int nw = a.nw;
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / G + 1;  // rows b, b + G, ... below T
     const uint32_t r_off = a.stage_bytes / 2;  // stage = [x row | residual row]
+    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -81,12 +85,6 @@ __global__ void __launch_bounds__(288, 2) fused_add_rmsnorm_fp8_kernel(FusedArgs
     const int H = a.H;
     const int nvec = H / VEC;
     const float Hf = (float)H;
-    WReg<__nv_bfloat16, VEC> wr[NCH];
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int v = c * NC + t;
-        if (v < nvec) wr[c].load(a.w, (int64_t)v * VEC);
-    }
 
     for (int64_t k = 0; k < nrows; ++k) {
         const int64_t row = b + k * G;
@@ -128,7 +126,7 @@ __global__ void __launch_bounds__(288, 2) fused_add_rmsnorm_fp8_kernel(FusedArgs
             float nf[VEC], wf[VEC];
             Elem<__nv_bfloat16>::unpack(hv[c], nf);
             if (in) {
-                wr[c].get(wf);
+                WSmem<__nv_bfloat16, VEC>::get(wsm, v, wf);
             } else {
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) wf[q] = 0.f;
@@ -167,9 +165,11 @@ __global__ void __launch_bounds__(288, 2) fused_add_rmsnorm_fp8_kernel(FusedArgs
 template <int NCH>
 static cudaError_t run(const Launch& L, const FusedArgs& a, cudaStream_t s) {
     auto k = fused_add_rmsnorm_fp8_kernel<NCH>;
-    cudaError_t e = allow_smem((const void*)k, L.smem);
+    const int threads = L.nw * 32 + 32;
+    int64_t grid = 0;
+    cudaError_t e = fit_grid((const void*)k, L, threads, &grid);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)L.grid, L.nw * 32 + 32, (size_t)L.smem, s>>>(a);
+    k<<<(unsigned)grid, threads, (size_t)L.smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -179,7 +179,7 @@ cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const v
     FusedArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(residual),
                 static_cast<const __nv_bfloat16*>(w), q, block_scale,
                 static_cast<__nv_bfloat16*>(normed), L.err, T, scale_ld, L.limit_ns, (int)H,
-                L.nw, L.stages, L.row_bytes, L.stage_bytes, eps};
+                L.nw, L.stages, L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off, eps};
     switch (L.nch) {
         case 1: return run<1>(L, a, s);
         case 2: return run<2>(L, a, s);

@@ -7,8 +7,8 @@
 // into a shared-memory ring with bulk copies; the consumer warps take a row out of the
 // ring into registers (16-byte vectors, lane-contiguous so every warp access is 512
 // contiguous bytes), release the stage, reduce sum(x^2) across the consumer warps, and
-// write y straight from registers; w stays in registers for the CTA's lifetime.  x is
-// read from HBM exactly once.
+// write y straight from registers.  w is copied to shared memory once per CTA.  x is read
+// from HBM exactly once.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
@@ -28,18 +28,22 @@ struct FwdArgs {
     int stages;
     uint32_t row_bytes;
     uint32_t stage_bytes;
+    uint32_t w_bytes;
+    uint32_t data_off;
     float eps;
 };
 
 template <typename TX, typename TW, int NCH>
-__global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
-    const Ring ring = ring_at(smem, a.stages, a.stage_bytes);
+    const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);
+    const uint8_t* wsm = smem + kRingHeader;
     const int nw = a.nw;
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / G + 1;  // rows b, b + G, ... below T
+    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -60,12 +64,6 @@ __global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
     const int nvec = a.H / VEC;
     const float Hf = (float)a.H;
     TX* __restrict__ Y = static_cast<TX*>(a.y);
-    WReg<TW, VEC> wr[NCH];
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int v = c * NC + t;
-        if (v < nvec) wr[c].load(static_cast<const TW*>(a.w), (int64_t)v * VEC);
-    }
 
     for (int64_t k = 0; k < nrows; ++k) {
         const int64_t row = b + k * G;
@@ -79,14 +77,18 @@ __global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
 
-        float ss = 0.f;
+        float ss0 = 0.f, ss1 = 0.f;  // two chains for ILP; a fixed order, same on every run
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             float f[VEC];
             Elem<TX>::unpack(xv[c], f);
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) ss = fmaf(f[q], f[q], ss);
+            for (int q = 0; q < VEC; q += 2) {
+                ss0 = fmaf(f[q], f[q], ss0);
+                ss1 = fmaf(f[q + 1], f[q + 1], ss1);
+            }
         }
+        float ss = __fadd_rn(ss0, ss1);
         if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
         const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
         if (t == 0) a.rstd[row] = rs;
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
             if (v < nvec) {
                 float f[VEC], wf[VEC];
                 Elem<TX>::unpack(xv[c], f);
-                wr[c].get(wf);
+                WSmem<TW, VEC>::get(wsm, v, wf);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) f[q] = __fmul_rn(__fmul_rn(f[q], rs), wf[q]);
                 st_stream(yr + (int64_t)v * VEC, Elem<TX>::pack(f));
@@ -110,9 +112,11 @@ __global__ void __launch_bounds__(288) rmsnorm_fwd_kernel(FwdArgs a) {
 template <typename TX, typename TW, int NCH>
 static cudaError_t run(const Launch& L, const FwdArgs& a, cudaStream_t s) {
     auto k = rmsnorm_fwd_kernel<TX, TW, NCH>;
-    cudaError_t e = allow_smem((const void*)k, L.smem);
+    const int threads = L.nw * 32 + 32;
+    int64_t grid = 0;
+    cudaError_t e = fit_grid((const void*)k, L, threads, &grid);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)L.grid, L.nw * 32 + 32, (size_t)L.smem, s>>>(a);
+    k<<<(unsigned)grid, threads, (size_t)L.smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -133,7 +137,7 @@ static cudaError_t dispatch(const Launch& L, const FwdArgs& a, cudaStream_t s) {
 cudaError_t launch_fwd(const Launch& L, const void* x, int x_dt, const void* w, int w_dt,
                        void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s) {
     FwdArgs a{x, w, y, rstd, L.err, T, L.limit_ns, (int)H, L.nw, L.stages, L.row_bytes,
-              L.stage_bytes, eps};
+              L.stage_bytes, L.w_bytes, L.data_off, eps};
     if (x_dt == 1 && w_dt == 1) return dispatch<__nv_bfloat16, __nv_bfloat16>(L, a, s);
     if (x_dt == 1 && w_dt == 0) return dispatch<__nv_bfloat16, float>(L, a, s);
     if (x_dt == 0 && w_dt == 0) return dispatch<float, float>(L, a, s);

@@ -14,9 +14,12 @@ struct Launch {
     int nch;             // 16-byte vectors per consumer lane per row (compile-time variant)
     int stages;          // ring depth
     int ctas_per_sm;     // CTAs per SM the grid is sized for
+    int sms;             // multiprocessors of the device
     uint32_t row_bytes;  // bytes of one input row
     uint32_t stage_bytes;// bytes of one stage (one or two padded rows)
-    int64_t grid;        // CTAs (backward: row chunks)
+    uint32_t w_bytes;    // bytes of the weight vector (copied to shared memory)
+    uint32_t data_off;   // shared-memory offset of the first stage
+    int64_t grid;        // CTAs planned (clamped to the kernel's occupancy at launch)
     int64_t smem;        // dynamic shared memory bytes per CTA
     unsigned* err;       // device error word (bounded waits that ran out)
     uint64_t limit_ns;   // time limit of every wait
@@ -39,7 +42,10 @@ cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const v
                          uint8_t* q, float* block_scale, int64_t scale_ld, void* normed,
                          int64_t T, int64_t H, float eps, cudaStream_t s);
 
-// Opt a kernel into more than 48 KiB of dynamic shared memory (once per kernel).
-cudaError_t allow_smem(const void* kernel, int64_t bytes);
+// Opts `kernel` into `smem` bytes of dynamic shared memory if that is above 48 KiB and
+// returns in *grid the planned grid clamped to what stays resident at once (SMs x the
+// kernel's occupancy at `threads` and `smem`), so a persistent grid never runs in two
+// waves.  Cached per device and kernel.
+cudaError_t fit_grid(const void* kernel, const Launch& L, int threads, int64_t* grid);
 
 }  // namespace rmsn

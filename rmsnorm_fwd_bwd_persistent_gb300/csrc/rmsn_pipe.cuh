@@ -98,6 +98,14 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
+// Copies `bytes` (a multiple of 8) of the weight vector into shared memory, all threads of
+// the CTA cooperating; made visible by the __syncthreads in ring_init.
+__device__ __forceinline__ void stage_weights(const void* w, uint8_t* dst, uint32_t bytes) {
+    const uint2* src = static_cast<const uint2*>(w);
+    uint2* d = reinterpret_cast<uint2*>(dst);
+    for (uint32_t i = threadIdx.x; i < bytes / 8; i += blockDim.x) d[i] = __ldg(src + i);
+}
+
 // Ring bookkeeping shared by the kernels: `stages` stages of `stage_bytes` each, placed
 // after the barrier block at the start of dynamic shared memory.
 struct Ring {
@@ -111,14 +119,15 @@ struct Ring {
 };
 
 // Dynamic shared memory layout: [full[S] | empty[S] | reduce slots (2 x 32 floats) |
-// abort flags (2 x 32 ints) | pad to 128 | S stages].
-constexpr int kRingHeader = 1024;  // bytes reserved before the stages (S <= 32)
+// abort flags (2 x 32 ints)] (kRingHeader bytes) [weights, padded to 128] [S stages].
+constexpr int kRingHeader = 1024;  // bytes reserved before the weights (S <= 32)
 
-__device__ __forceinline__ Ring ring_at(uint8_t* smem, int stages, uint32_t stage_bytes) {
+__device__ __forceinline__ Ring ring_at(uint8_t* smem, int stages, uint32_t stage_bytes,
+                                        uint32_t data_offset) {
     Ring r;
     r.full = reinterpret_cast<uint64_t*>(smem);
     r.empty = r.full + 32;
-    r.data = smem + kRingHeader;
+    r.data = smem + data_offset;
     r.stages = stages;
     r.stage_bytes = stage_bytes;
     return r;

@@ -195,3 +195,15 @@ def test_errors_on_device():
     with pytest.raises(rmsn.RmsnError):
         rmsn.fused_add_rmsnorm_fp8_block_quant(x[:, :200].contiguous(), x[:, :200].contiguous(),
                                                w[:200].contiguous())
+
+
+def test_kernel_reuse_across_shared_memory_sizes():
+    """The same kernel variant (bf16 x, fp32 w, 3 vectors per lane) runs at H = 5120 and
+    H = 6144 with different shared-memory sizes; using the larger size again after the
+    smaller one must still launch (the per-kernel limit is never lowered)."""
+    for H in (5120, 6144, 5120):
+        x, dy, w = wl.fwd_bwd_inputs(_wl(wl.MAIN_BF16, 40, H, torch.bfloat16, torch.float32), DEV,
+                                     seed=H)
+        r = P.check_fwd(x, w, 1e-6)
+        P.assert_ok(r, f"fwd H={H}")
+        P.assert_ok(P.check_bwd(dy, x, w, r["_rstd_dev"]), f"bwd H={H}")
