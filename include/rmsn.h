@@ -65,7 +65,9 @@ typedef enum {
     RMSN_ERR_MISALIGNED = 3,          /* a pointer violates its alignment */
     RMSN_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace smaller than rmsnorm_bwd_workspace_bytes */
     RMSN_ERR_CUDA = 5,                /* a CUDA runtime call or a launch failed */
-    RMSN_ERR_DEVICE_TIMEOUT = 6       /* rmsn_device_status: a kernel's bounded wait ran out */
+    RMSN_ERR_DEVICE_TIMEOUT = 6,      /* rmsn_device_status: a kernel's bounded wait ran out */
+    RMSN_ERR_SCRATCH_LIMIT = 7        /* rmsnorm_bwd_noalloc: the call needs more scratch than
+                                         the library's fixed RMSN_NOALLOC_SCRATCH_BYTES */
 } rmsn_status;
 
 #define RMSN_MAX_H 16384
@@ -238,6 +240,38 @@ int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages)
  * when a CTA gave up) and returns RMSN_OK if it was 0, RMSN_ERR_DEVICE_TIMEOUT otherwise.
  * ---------------------------------------------------------------------------------- */
 int rmsn_device_status(rmsn_stream_t stream, unsigned* flags);
+
+/* ------------------------------------------------------------------------------------
+ * rmsnorm_bwd_noalloc -- the deterministic rmsnorm_bwd for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this entry point.  rmsnorm_bwd needs a caller-owned
+ * scratch workspace; some callers cannot provide one at the point of the call: a
+ * framework whose allocator hands out all device memory up front from its own pool, a
+ * latency-critical loop in which cudaMalloc's implicit device synchronization would stall
+ * the pipeline, or a plain C caller with no allocator to size and own a workspace.  This
+ * entry point keeps the workspace in a fixed array of RMSN_NOALLOC_SCRATCH_BYTES that the
+ * library places in device memory when it is loaded (every GPU the library is used on
+ * holds that array until the process exits); it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Arguments, layouts and results are those of rmsnorm_bwd with deterministic = 1 (the
+ * same kernels, so the same dx and, for the same device, dw).  The caller still provides
+ * dy, x, w, rstd, dx and dw.
+ *   - Returns RMSN_ERR_SCRATCH_LIMIT (nothing enqueued) when the call would need more than
+ *     RMSN_NOALLOC_SCRATCH_BYTES of scratch, i.e. when 8 * H * min(T, SMs * 2) exceeds it
+ *     (on a 152-SM GB300: H <= 6144 always fits; H = 8192 fits up to T = 256).
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls in the process share the one array.  Every call writes all the scratch it
+ *     reads, so nothing has to start at zero, but calls that overlap on the GPU (on
+ *     different streams, or from several host threads without ordering) race on the
+ *     array and produce wrong dw: order them on one stream.
+ * ---------------------------------------------------------------------------------- */
+#define RMSN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int rmsnorm_bwd_noalloc(const void* dy, const void* x, int x_dtype, const void* w, int w_dtype,
+                        const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
+                        int compensated, rmsn_stream_t stream);
 
 #ifdef __cplusplus
 }

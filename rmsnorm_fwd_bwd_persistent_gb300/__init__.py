@@ -86,6 +86,9 @@ def load_library():
         L.rmsn_set_policy.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.rmsn_device_status.restype = ctypes.c_int
         L.rmsn_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint)]
+        L.rmsnorm_bwd_noalloc.restype = ctypes.c_int
+        L.rmsnorm_bwd_noalloc.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp,
+                                          _vp, _i64, _i64, ctypes.c_int, _vp]
         _lib = L
         return _lib
 

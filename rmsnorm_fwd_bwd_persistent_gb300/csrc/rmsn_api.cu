@@ -262,6 +262,9 @@ const char* rmsn_status_string(int status) {
         case RMSN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than rmsnorm_bwd_workspace_bytes";
         case RMSN_ERR_CUDA: return "CUDA error (launch or runtime call failed)";
         case RMSN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out (device error word set)";
+        case RMSN_ERR_SCRATCH_LIMIT:
+            return "rmsnorm_bwd_noalloc: this T and H need more scratch than its fixed 16 MiB "
+                   "(use rmsnorm_bwd with a caller workspace)";
         default: return "unknown status";
     }
 }
@@ -397,3 +400,60 @@ int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------- allocation-free backward
+// Scratch of rmsnorm_bwd_noalloc, for callers that cannot allocate a workspace (see
+// include/rmsn.h).  It lives in device memory reserved when the library is loaded; the
+// name is a host-side stand-in, so the device address is looked up per device below and
+// only that address is handed to the kernels.
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[RMSN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the scratch array on `dev` (which must be current); looked up once per
+// device.  nullptr if the lookup fails.
+void* noalloc_scratch(int dev) {
+    static std::atomic<void*> addr[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    addr[dev].store(ptr, std::memory_order_release);
+    return ptr;
+}
+
+}  // namespace
+
+extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, int x_dtype, const void* w,
+                                   int w_dtype, const float* rstd, void* dx, float* dw, int64_t T,
+                                   int64_t H, int compensated, rmsn_stream_t stream) {
+    if (!valid_dtype(x_dtype) || !valid_dtype(w_dtype) || T < 0) return RMSN_ERR_INVALID_ARG;
+    if (H <= 0 || H > RMSN_MAX_H || H % (16 / esize(x_dtype)) != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (!dw) return RMSN_ERR_INVALID_ARG;
+    if (!aligned(dw, 16)) return RMSN_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) return from_cuda(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s));
+    if (!dy || !x || !w || !rstd || !dx) return RMSN_ERR_INVALID_ARG;
+    if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(w, 16) || !aligned(dx, 16) ||
+        !aligned(rstd, 4))
+        return RMSN_ERR_MISALIGNED;
+    Launch L{};
+    int64_t need = 0;
+    int st = plan_current(RMSN_OP_BWD, T, H, x_dtype, w_dtype, &L, &need);
+    if (st != RMSN_OK) return st;
+    if (need > (int64_t)RMSN_NOALLOC_SCRATCH_BYTES) return RMSN_ERR_SCRATCH_LIMIT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSN_ERR_CUDA;
+    }
+    void* scratch = noalloc_scratch(dev);
+    if (!scratch) return RMSN_ERR_CUDA;
+    return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
+                                      /*deterministic=*/1, compensated,
+                                      static_cast<float*>(scratch), s));
+}

@@ -43,7 +43,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, 7):
+    for s in range(0, 8):
         assert rmsn.rmsn_status_string(s) and rmsn.rmsn_status_string(s) != "unknown status"
     assert rmsn.rmsn_status_string(99) == "unknown status"
 
