@@ -142,7 +142,7 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     const int64_t row_bytes = H * esize(x_dt);
     const int64_t row_pad = cdiv(row_bytes, 128) * 128;
     const int64_t stage_bytes = (op == RMSN_OP_FWD) ? row_pad : 2 * row_pad;
-    const int64_t w_bytes = H * esize(w_dt);
+    const int64_t w_bytes = H * 4;  // w is staged in shared memory as FP32
     const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
     int cps = P.ctas_per_sm;
     auto stages_for = [&](int c) -> int64_t {

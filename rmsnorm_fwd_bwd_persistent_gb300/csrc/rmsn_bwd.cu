@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / nch + 1;  // rows b, b + n, ... below T
     const uint32_t dy_off = a.stage_bytes / 2;  // stage = [x row | dy row], each padded
-    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
+    stage_weights_f32<VEC>(static_cast<const TW*>(a.w), a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -94,16 +94,17 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     const float Hf = (float)H;
     TX* __restrict__ DX = static_cast<TX*>(a.dx);
 
+    constexpr int NP = Pairs<TX>::NP;
     constexpr int NB = COMP ? 1 : NCH;  // block-sum registers (blocked mode only)
-    float hi[NCH][VEC], lo[NCH][VEC], blk[NB][VEC];
+    f2 hi[NCH][NP], lo[NCH][NP], blk[NB][NP];
 #pragma unroll
     for (int c = 0; c < NCH; ++c)
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) hi[c][q] = lo[c][q] = 0.f;
+        for (int i = 0; i < NP; ++i) hi[c][i] = lo[c][i] = f2_splat(0.f);
 #pragma unroll
     for (int c = 0; c < NB; ++c)
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) blk[c][q] = 0.f;
+        for (int i = 0; i < NP; ++i) blk[c][i] = f2_splat(0.f);
 
     int64_t k = 0;
     for (; k < nrows; ++k) {
@@ -112,45 +113,48 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
         const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
         const uint8_t* st = ring.stage((int)(k % ring.stages));
 
-        // pass 1: sum_j (dy_j * w_j) * x_j over the row (x, dy read from the stage)
-        float dot = 0.f;
+        // pass 1: sum_j (dy_j * w_j) * x_j over the row (x, dy read from the stage), in two
+        // chains (even and odd elements) added at the end
+        f2 dot2 = f2_splat(0.f);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (ok && v < nvec) {
-                float xf[VEC], df[VEC], wf[VEC];
-                Elem<TX>::unpack(lds128(st + (size_t)v * 16), xf);
-                Elem<TX>::unpack(lds128(st + dy_off + (size_t)v * 16), df);
-                WSmem<TW, VEC>::get(wsm, v, wf);
+                f2 xp[NP], dp[NP], wp[NP];
+                Pairs<TX>::get(lds128(st + (size_t)v * 16), xp);
+                Pairs<TX>::get(lds128(st + dy_off + (size_t)v * 16), dp);
+                w_pairs<NP>(wsm, nvec, v, wp);
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) dot = fmaf(__fmul_rn(df[q], wf[q]), xf[q], dot);
+                for (int i = 0; i < NP; ++i) dot2 = fma2(mul2(dp[i], wp[i]), xp[i], dot2);
             }
         }
+        float dot = __fadd_rn(f2_lo(dot2), f2_hi(dot2));
         if (!consumer_sum(smem, dot, ok, nw, (int)(k & 1))) break;
         // c = mean_j(g_j * xhat_j) = rstd * sum_j(g_j * x_j) / H
         const float cm = __fdiv_rn(__fmul_rn(rs, dot), Hf);
+        const f2 rs2 = f2_splat(rs), ncm2 = f2_splat(-cm);
 
-        // pass 2: dx and the dw accumulators (x, dy read from the stage again)
+        // pass 2: dx = rstd * (g - xhat * c) and the dw accumulators (x, dy read again)
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (v < nvec) {
-                float xf[VEC], df[VEC], wf[VEC], o[VEC];
-                Elem<TX>::unpack(lds128(st + (size_t)v * 16), xf);
-                Elem<TX>::unpack(lds128(st + dy_off + (size_t)v * 16), df);
-                WSmem<TW, VEC>::get(wsm, v, wf);
+                f2 xp[NP], dp[NP], wp[NP], o[NP];
+                Pairs<TX>::get(lds128(st + (size_t)v * 16), xp);
+                Pairs<TX>::get(lds128(st + dy_off + (size_t)v * 16), dp);
+                w_pairs<NP>(wsm, nvec, v, wp);
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) {
-                    const float xh = __fmul_rn(xf[q], rs);
-                    const float g = __fmul_rn(df[q], wf[q]);
-                    o[q] = __fmul_rn(rs, fmaf(-xh, cm, g));
+                for (int i = 0; i < NP; ++i) {
+                    const f2 xh = mul2(xp[i], rs2);
+                    const f2 g = mul2(dp[i], wp[i]);
+                    o[i] = mul2(rs2, fma2(xh, ncm2, g));
                     if constexpr (COMP) {
-                        comp_add(hi[c][q], lo[c][q], __fmul_rn(df[q], xh));
+                        comp_add2(hi[c][i], lo[c][i], mul2(dp[i], xh));
                     } else {
-                        blk[c][q] = fmaf(df[q], xh, blk[c][q]);
+                        blk[c][i] = fma2(dp[i], xh, blk[c][i]);
                     }
                 }
-                st_stream(DX + row * H + (int64_t)v * VEC, Elem<TX>::pack(o));
+                st_stream(DX + row * H + (int64_t)v * VEC, Pairs<TX>::put(o));
             }
         }
         ring_release(ring, k);  // every consumer warp has read the stage twice
@@ -159,9 +163,9 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
                 for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) {
-                        comp_add(hi[c][q], lo[c][q], blk[c][q]);
-                        blk[c][q] = 0.f;
+                    for (int i = 0; i < NP; ++i) {
+                        comp_add2(hi[c][i], lo[c][i], blk[c][i]);
+                        blk[c][i] = f2_splat(0.f);
                     }
             }
         }
@@ -172,11 +176,11 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) comp_add(hi[c][q], lo[c][q], blk[c][q]);
+                for (int i = 0; i < NP; ++i) comp_add2(hi[c][i], lo[c][i], blk[c][i]);
         }
     }
 
-    // ---- emit the chunk's partial
+    // ---- emit the chunk's partial (pairs are consecutive columns)
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
         const int v = c * NC + t;
@@ -184,16 +188,18 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
             const int col0 = v * VEC;
             if (a.atomic) {
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) atomicAdd(a.dw + col0 + q, __fadd_rn(hi[c][q], lo[c][q]));
+                for (int i = 0; i < NP; ++i) {
+                    const f2 sum = add2(hi[c][i], lo[c][i]);
+                    atomicAdd(a.dw + col0 + 2 * i, f2_lo(sum));
+                    atomicAdd(a.dw + col0 + 2 * i + 1, f2_hi(sum));
+                }
             } else {
-                float* dh = a.ws + (int64_t)blockIdx.x * H + col0;
-                float* dl = dh + nch * H;
+                f2* dh = reinterpret_cast<f2*>(a.ws + (int64_t)blockIdx.x * H + col0);
+                f2* dl = reinterpret_cast<f2*>(a.ws + (nch + (int64_t)blockIdx.x) * H + col0);
 #pragma unroll
-                for (int q = 0; q < VEC; q += 4) {
-                    *reinterpret_cast<float4*>(dh + q) =
-                        make_float4(hi[c][q], hi[c][q + 1], hi[c][q + 2], hi[c][q + 3]);
-                    *reinterpret_cast<float4*>(dl + q) =
-                        make_float4(lo[c][q], lo[c][q + 1], lo[c][q + 2], lo[c][q + 3]);
+                for (int i = 0; i < NP; i += 2) {
+                    *reinterpret_cast<ulonglong2*>(dh + i) = make_ulonglong2(hi[c][i], hi[c][i + 1]);
+                    *reinterpret_cast<ulonglong2*>(dl + i) = make_ulonglong2(lo[c][i], lo[c][i + 1]);
                 }
             }
         }

@@ -63,52 +63,98 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
     __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
-// The weights beside one 16-byte vector v of x, read from the copy of w in shared memory
-// (VEC = 16 / sizeof(x) weights of type TW, at byte offset v * VEC * sizeof(TW)).
-template <typename TW, int VEC>
-struct WSmem;
+// ------------------------------------------------------------------ paired FP32 arithmetic
+// Blackwell executes two IEEE binary32 operations per instruction on a 64-bit register
+// pair (mul/fma/add/sub .rn.f32x2).  Each half is rounded exactly as the scalar operation
+// would be, so the results are bit-identical to __fmul_rn / fmaf / __fadd_rn / __fsub_rn
+// element by element; only the instruction count halves.  A pair holds (even, odd)
+// elements in (low, high) halves.
+using f2 = uint64_t;
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f2 f2_splat(float v) { return f2_make(v, v); }
+__device__ __forceinline__ float f2_lo(f2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(f2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    f2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// A 16-byte vector of x as FP32 pairs (NP pairs) and back (one rounding to x's type).
+template <typename T>
+struct Pairs;
 
 template <>
-struct WSmem<__nv_bfloat16, 8> {
-    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[8]) {
-        uint4 u;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 16)));
-        Elem<__nv_bfloat16>::unpack(u, f);
+struct Pairs<float> {
+    static constexpr int NP = 2;
+    __device__ __forceinline__ static void get(const uint4& v, f2 (&p)[2]) {
+        p[0] = f2_make(__uint_as_float(v.x), __uint_as_float(v.y));
+        p[1] = f2_make(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ __forceinline__ static uint4 put(const f2 (&p)[2]) {
+        return make_uint4(__float_as_uint(f2_lo(p[0])), __float_as_uint(f2_hi(p[0])),
+                          __float_as_uint(f2_lo(p[1])), __float_as_uint(f2_hi(p[1])));
     }
 };
+
 template <>
-struct WSmem<__nv_bfloat16, 4> {
-    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[4]) {
-        uint32_t a, b;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                     : "=r"(a), "=r"(b)
-                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 8)));
-        f[0] = bf16_lo(a); f[1] = bf16_hi(a);
-        f[2] = bf16_lo(b); f[3] = bf16_hi(b);
+struct Pairs<__nv_bfloat16> {
+    static constexpr int NP = 4;
+    __device__ __forceinline__ static f2 word(uint32_t u) { return f2_make(bf16_lo(u), bf16_hi(u)); }
+    __device__ __forceinline__ static void get(const uint4& v, f2 (&p)[4]) {
+        p[0] = word(v.x);
+        p[1] = word(v.y);
+        p[2] = word(v.z);
+        p[3] = word(v.w);
+    }
+    __device__ __forceinline__ static uint32_t round_word(f2 v) {
+        return pack_bf16x2(f2_lo(v), f2_hi(v));
+    }
+    __device__ __forceinline__ static uint4 put(const f2 (&p)[4]) {
+        return make_uint4(round_word(p[0]), round_word(p[1]), round_word(p[2]), round_word(p[3]));
     }
 };
-template <>
-struct WSmem<float, 8> {
-    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[8]) {
-        const uint32_t addr = (uint32_t)__cvta_generic_to_shared(w + (size_t)v * 32);
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
-                     : "r"(addr));
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
-                     : "r"(addr + 16));
-    }
-};
-template <>
-struct WSmem<float, 4> {
-    __device__ __forceinline__ static void get(const uint8_t* w, int v, float (&f)[4]) {
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
-                     : "r"((uint32_t)__cvta_generic_to_shared(w + (size_t)v * 16)));
-    }
-};
+
+// The weights beside 16-byte vector v of x as FP32 pairs, read from the planar FP32 copy
+// of w in shared memory (stage_weights_f32): plane q holds pairs 2q and 2q+1 of every
+// vector at byte offset (q * nvec + v) * 16.
+template <int NP>
+__device__ __forceinline__ void w_pairs(const uint8_t* wsm, int nvec, int v, f2 (&p)[NP]) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(wsm);
+#pragma unroll
+    for (int q = 0; q < NP / 2; ++q)
+        asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];"
+                     : "=l"(p[2 * q]), "=l"(p[2 * q + 1])
+                     : "r"(base + (uint32_t)(q * nvec + v) * 16));
+}
 
 // ------------------------------------------------------------------ compensated sums
 // Error-free transformation of a + b (Knuth's TwoSum): s + e == a + b exactly.
@@ -134,6 +180,21 @@ __device__ __forceinline__ void comp_merge(float& hi, float& lo, float h2, float
     two_sum(hi, h2, s, e);
     hi = s;
     lo = __fadd_rn(lo, __fadd_rn(e, l2));
+}
+
+// TwoSum on both halves of a pair: s + e == a + b exactly, per half.
+__device__ __forceinline__ void two_sum2(f2 a, f2 b, f2& s, f2& e) {
+    s = add2(a, b);
+    const f2 bb = sub2(s, a);
+    e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+// (hi, lo) += v on both halves
+__device__ __forceinline__ void comp_add2(f2& hi, f2& lo, f2 v) {
+    f2 s, e;
+    two_sum2(hi, v, s, e);
+    hi = s;
+    lo = add2(lo, e);
 }
 
 }  // namespace rmsn

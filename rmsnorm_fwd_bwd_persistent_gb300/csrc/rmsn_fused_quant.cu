@@ -7,8 +7,8 @@
 //   n = bf16((h * rstd) * w)        -> written to normed
 //   per block b of 128 columns: amax = max|n|, scale = amax / 448 (IEEE FP32)
 //                                   -> block_scale[b * ld + row]
-//   q = e4m3_rn_satfinite(n / scale) (IEEE FP32 division; a block with amax 0 keeps the
-//                                   signed zero of each element)
+//   q = e4m3_rn_satfinite(n / scale) (the code of the IEEE FP32 quotient; a block with
+//                                   amax 0 keeps the signed zero of each element)
 // The quantization reads the bf16-rounded n, so re-quantizing the normed output gives
 // back q exactly.  With 16-byte vectors of 8 bf16 and lane-contiguous vectors
 // (v = c * NC + t), a 128-column block is held by 16 consecutive lanes of one warp, so its
@@ -17,7 +17,8 @@
 // The page's kernel runs one CTA per row in a single wave; here the grid is persistent:
 // CTA b streams the rows b, b + G, ... (x and residual) through a shared-memory ring
 // filled by bulk copies, and its consumer warps share one row at a time; w is copied to
-// shared memory once per CTA.
+// shared memory (as FP32) once per CTA.  The arithmetic runs on FP32 pairs (two IEEE
+// operations per instruction, each rounded as its scalar form would be).
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
@@ -49,6 +50,24 @@ struct FusedArgs {
 __device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
+__device__ __forceinline__ uint32_t to_e4m3x2(f2 v) { return to_e4m3x2(f2_lo(v), f2_hi(v)); }
+
+// E4M3 codes of RN(n / s) for a pair of bf16-rounded normed values n, where s > 0 is the
+// block scale and y = RN(1 / s) (s and y normal).  The IEEE quotient Q = RN(n / s) is not
+// formed directly: q0 = RN(n * y) satisfies |q0 - Q| < 3.01 * 2^-24 * |q0| (y is within
+// 2^-24 relative of 1/s, and each rounding adds at most 2^-24 relative), so
+// lo = RN(q0 * (1 - 2^-21)) and hi = RN(q0 * (1 + 2^-21)) bracket Q.  The conversion is
+// monotone, so if lo and hi give the same code, that is the code of Q.  Otherwise (when Q
+// lies within a few units in the last place of an E4M3 rounding boundary: about one
+// element in 10^5) the code is taken from the IEEE division itself.  Values below 2^-100
+// in magnitude have the signed-zero code on every path.
+__device__ __forceinline__ uint32_t quotient_codes(f2 n, f2 y, float s) {
+    const f2 q0 = mul2(n, y);
+    const uint32_t clo = to_e4m3x2(mul2(q0, f2_splat(1.0f - 0x1p-21f)));
+    const uint32_t chi = to_e4m3x2(mul2(q0, f2_splat(1.0f + 0x1p-21f)));
+    if (clo == chi) return clo;
+    return to_e4m3x2(__fdiv_rn(f2_lo(n), s), __fdiv_rn(f2_hi(n), s));
+}
 
 template <int NCH>
 __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs a) {
@@ -61,7 +80,7 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / G + 1;  // rows b, b + G, ... below T
     const uint32_t r_off = a.stage_bytes / 2;  // stage = [x row | residual row]
-    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
+    stage_weights_f32<VEC>(a.w, a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -85,6 +104,7 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
     const int H = a.H;
     const int nvec = H / VEC;
     const float Hf = (float)H;
+    constexpr int NP = 4;  // FP32 pairs per 16-byte vector of bf16
 
     for (int64_t k = 0; k < nrows; ++k) {
         const int64_t row = b + k * G;
@@ -92,72 +112,77 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
         const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
         const uint8_t* st = ring.stage((int)(k % ring.stages));
         uint4 hv[NCH];
-        float ss = 0.f;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             const bool in = ok && v < nvec;
-            const uint4 xv = in ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-            const uint4 rv = in ? lds128(st + r_off + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-            float xf[VEC], rf[VEC];
-            Elem<__nv_bfloat16>::unpack(xv, xf);
-            Elem<__nv_bfloat16>::unpack(rv, rf);
+            f2 xp[NP], rp[NP];
+            Pairs<__nv_bfloat16>::get(in ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0), xp);
+            Pairs<__nv_bfloat16>::get(in ? lds128(st + r_off + (size_t)v * 16) : make_uint4(0, 0, 0, 0), rp);
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) rf[q] = __fadd_rn(xf[q], rf[q]);
-            hv[c] = Elem<__nv_bfloat16>::pack(rf);  // h rounded once to bf16
+            for (int i = 0; i < NP; ++i) rp[i] = add2(xp[i], rp[i]);
+            hv[c] = Pairs<__nv_bfloat16>::put(rp);  // h rounded once to bf16
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
+        f2 ss2 = f2_splat(0.f);  // even and odd elements, added at the end
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (ok && v < nvec) st_stream(a.res + base + (int64_t)v * VEC, hv[c]);
-            float hf[VEC];
-            Elem<__nv_bfloat16>::unpack(hv[c], hf);
+            f2 hp[NP];
+            Pairs<__nv_bfloat16>::get(hv[c], hp);
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) ss = fmaf(hf[q], hf[q], ss);
+            for (int i = 0; i < NP; ++i) ss2 = fma2(hp[i], hp[i], ss2);
         }
+        float ss = __fadd_rn(f2_lo(ss2), f2_hi(ss2));
         if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
         const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
+        const f2 rs2 = f2_splat(rs);
 
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             const bool in = v < nvec;  // uniform over each 16-lane block (H % 128 == 0)
-            float nf[VEC], wf[VEC];
-            Elem<__nv_bfloat16>::unpack(hv[c], nf);
+            f2 np_[NP], wp[NP];
+            Pairs<__nv_bfloat16>::get(hv[c], np_);
             if (in) {
-                WSmem<__nv_bfloat16, VEC>::get(wsm, v, wf);
+                w_pairs<NP>(wsm, nvec, v, wp);
             } else {
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) wf[q] = 0.f;
+                for (int i = 0; i < NP; ++i) wp[i] = f2_splat(0.f);
             }
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) nf[q] = __fmul_rn(__fmul_rn(nf[q], rs), wf[q]);
-            const uint4 nv = Elem<__nv_bfloat16>::pack(nf);
+            for (int i = 0; i < NP; ++i) np_[i] = mul2(mul2(np_[i], rs2), wp[i]);
+            const uint4 nv = Pairs<__nv_bfloat16>::put(np_);
             if (in) st_stream(a.normed + base + (int64_t)v * VEC, nv);
-            Elem<__nv_bfloat16>::unpack(nv, nf);  // the bf16-rounded normed values
+            Pairs<__nv_bfloat16>::get(nv, np_);  // the bf16-rounded normed values
 
             float amax = 0.f;
 #pragma unroll
-            for (int q = 0; q < VEC; ++q) amax = fmaxf(amax, fabsf(nf[q]));
+            for (int i = 0; i < NP; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(f2_lo(np_[i])), fabsf(f2_hi(np_[i]))));
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             const float scale = __fdiv_rn(amax, 448.0f);
             if (in && (t & 15) == 0) a.scale[(int64_t)(v >> 4) * a.ld + row] = scale;
 
-            uint32_t packed[2];
+            uint32_t codes[NP];
+            if (amax >= 0x1p-100f) {
+                const f2 y2 = f2_splat(__frcp_rn(scale));
 #pragma unroll
-            for (int q = 0; q < VEC; q += 4) {
-                float qv[4];
+                for (int i = 0; i < NP; ++i) codes[i] = quotient_codes(np_[i], y2, scale);
+            } else if (scale > 0.f) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    qv[u] = (scale > 0.f) ? __fdiv_rn(nf[q + u], scale) : nf[q + u];
-                packed[q / 4] = to_e4m3x2(qv[0], qv[1]) | (to_e4m3x2(qv[2], qv[3]) << 16);
+                for (int i = 0; i < NP; ++i)
+                    codes[i] = to_e4m3x2(__fdiv_rn(f2_lo(np_[i]), scale), __fdiv_rn(f2_hi(np_[i]), scale));
+            } else {  // amax == 0: the signed zero of each element
+#pragma unroll
+                for (int i = 0; i < NP; ++i) codes[i] = to_e4m3x2(np_[i]);
             }
             if (in)
                 __stcs(reinterpret_cast<uint2*>(a.q + base + (int64_t)v * VEC),
-                       make_uint2(packed[0], packed[1]));
+                       make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16)));
         }
     }
 }

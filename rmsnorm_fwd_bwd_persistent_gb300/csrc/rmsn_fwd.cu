@@ -7,8 +7,9 @@
 // into a shared-memory ring with bulk copies; the consumer warps take a row out of the
 // ring into registers (16-byte vectors, lane-contiguous so every warp access is 512
 // contiguous bytes), release the stage, reduce sum(x^2) across the consumer warps, and
-// write y straight from registers.  w is copied to shared memory once per CTA.  x is read
-// from HBM exactly once.
+// write y straight from registers.  w is copied to shared memory (as FP32) once per CTA.
+// The arithmetic runs on FP32 pairs (two IEEE operations per instruction, each rounded as
+// its scalar form would be).  x is read from HBM exactly once.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / G + 1;  // rows b, b + G, ... below T
-    stage_weights(a.w, smem + kRingHeader, a.w_bytes);
+    stage_weights_f32<VEC>(static_cast<const TW*>(a.w), a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
     if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
@@ -77,33 +78,35 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
 
-        float ss0 = 0.f, ss1 = 0.f;  // two chains for ILP; a fixed order, same on every run
+        // sum of squares in two chains (even and odd elements), one pair instruction per two
+        // elements; the chains are added at the end (a fixed order, same on every run)
+        constexpr int NP = Pairs<TX>::NP;
+        f2 ss2 = f2_splat(0.f);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            float f[VEC];
-            Elem<TX>::unpack(xv[c], f);
+            f2 p[NP];
+            Pairs<TX>::get(xv[c], p);
 #pragma unroll
-            for (int q = 0; q < VEC; q += 2) {
-                ss0 = fmaf(f[q], f[q], ss0);
-                ss1 = fmaf(f[q + 1], f[q + 1], ss1);
-            }
+            for (int i = 0; i < NP; ++i) ss2 = fma2(p[i], p[i], ss2);
         }
-        float ss = __fadd_rn(ss0, ss1);
+        float ss = __fadd_rn(f2_lo(ss2), f2_hi(ss2));
         if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
         const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
         if (t == 0) a.rstd[row] = rs;
 
+        // y = (x * rstd) * w, two elements per instruction, rounded once to x's type
+        const f2 rs2 = f2_splat(rs);
         TX* yr = Y + row * a.H;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (v < nvec) {
-                float f[VEC], wf[VEC];
-                Elem<TX>::unpack(xv[c], f);
-                WSmem<TW, VEC>::get(wsm, v, wf);
+                f2 p[NP], wp[NP];
+                Pairs<TX>::get(xv[c], p);
+                w_pairs<NP>(wsm, nvec, v, wp);
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) f[q] = __fmul_rn(__fmul_rn(f[q], rs), wf[q]);
-                st_stream(yr + (int64_t)v * VEC, Elem<TX>::pack(f));
+                for (int i = 0; i < NP; ++i) p[i] = mul2(mul2(p[i], rs2), wp[i]);
+                st_stream(yr + (int64_t)v * VEC, Pairs<TX>::put(p));
             }
         }
     }

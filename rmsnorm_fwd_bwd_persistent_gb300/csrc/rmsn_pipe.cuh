@@ -14,6 +14,7 @@
 // (again bounded) for the copies it issued.  No wait spins forever and nothing traps.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -98,12 +99,31 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
-// Copies `bytes` (a multiple of 8) of the weight vector into shared memory, all threads of
-// the CTA cooperating; made visible by the __syncthreads in ring_init.
-__device__ __forceinline__ void stage_weights(const void* w, uint8_t* dst, uint32_t bytes) {
-    const uint2* src = static_cast<const uint2*>(w);
-    uint2* d = reinterpret_cast<uint2*>(dst);
-    for (uint32_t i = threadIdx.x; i < bytes / 8; i += blockDim.x) d[i] = __ldg(src + i);
+// Copies the H weights into shared memory as FP32 (bf16 weights are widened exactly), all
+// threads of the CTA cooperating; made visible by the __syncthreads in ring_init.
+// Layout for a row split into 16-byte vectors of VEC elements: P = VEC / 4 planes of
+// 16-byte slots; slot (plane q, vector v) at float4 index q * (H / VEC) + v holds weights
+// v*VEC + 4q .. v*VEC + 4q + 3, so consecutive lanes read consecutive 16-byte slots.
+template <int VEC>
+__device__ __forceinline__ void stage_weights_f32(const float* w, int H, uint8_t* dst) {
+    constexpr int P = VEC / 4;
+    const int nvec = H / VEC;
+    const float4* src = reinterpret_cast<const float4*>(w);
+    float4* d = reinterpret_cast<float4*>(dst);
+    for (int g = threadIdx.x; g < H / 4; g += blockDim.x) d[(g % P) * nvec + g / P] = __ldg(src + g);
+}
+template <int VEC>
+__device__ __forceinline__ void stage_weights_f32(const __nv_bfloat16* w, int H, uint8_t* dst) {
+    constexpr int P = VEC / 4;
+    const int nvec = H / VEC;
+    const uint2* src = reinterpret_cast<const uint2*>(w);
+    float4* d = reinterpret_cast<float4*>(dst);
+    for (int g = threadIdx.x; g < H / 4; g += blockDim.x) {
+        const uint2 u = __ldg(src + g);
+        d[(g % P) * nvec + g / P] =
+            make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    }
 }
 
 // Ring bookkeeping shared by the kernels: `stages` stages of `stage_bytes` each, placed

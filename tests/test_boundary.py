@@ -116,7 +116,7 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
         row = H * (2 if xd == 1 else 4)
         stage = -(-row // 128) * 128 * (1 if op == rmsn.OP_FWD else 2)
-        wpad = -(-(H * (2 if wd == 1 else 4)) // 128) * 128        # w staged in shared memory
+        wpad = -(-(H * 4) // 128) * 128                           # w staged as FP32 in smem
         assert p["stages"] >= 1 and p["smem_bytes"] == 1024 + wpad + p["stages"] * stage
         assert p["ctas_per_sm"] * (p["smem_bytes"] + 1024) <= 233472  # fits the SM
         if p["ctas_per_sm"] > 1:
