@@ -37,9 +37,9 @@ struct Policy {
 
 // Per op: FWD, BWD, FUSED.
 constexpr Policy kDefaultPolicy[3] = {
-    {0, 4, 3, 4, 16},  // forward: small CTAs, 4 per SM, a shallow ring
-    {0, 2, 3, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
-    {0, 4, 3, 4, 8},   // fused quant
+    {0, 4, 2, 4, 16},  // forward: small CTAs, 4 per SM, two stages each
+    {0, 2, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
+    {0, 3, 2, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM
 };
 Policy g_policy[3] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2]};
 std::mutex g_mu;
@@ -113,8 +113,8 @@ int pick_nch(const int (&set)[N], int64_t need) {
 // lanes hold about `target_nch` 16-byte vectors of a row each; the chunk variant is the
 // smallest compiled count that covers the row.  Shared memory per CTA: the ring header,
 // the weight vector, and as many stages (<= max_stages) as the CTA's share of the SM
-// holds; fewer CTAs per SM if a share cannot hold two stages.  The grid is clamped again
-// at launch to what is resident at once (fit_grid).
+// holds (the backward at least two); fewer CTAs per SM if a share cannot hold two stages.
+// The grid is clamped again at launch to what is resident at once (fit_grid).
 int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem_sm,
          int64_t smem_cta, Launch* L, int64_t* ws_bytes) {
     if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
@@ -150,10 +150,12 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
         if (share > smem_cta) share = smem_cta;
         return (share - data_off) / stage_bytes;
     };
+    // the backward holds two rows' stages at once (it takes rows two at a time)
+    const int64_t min_stages = (op == RMSN_OP_BWD) ? 2 : 1;
     while (cps > 1 && stages_for(cps) < 2) --cps;
     int64_t stages = stages_for(cps);
-    if (stages > P.max_stages) stages = P.max_stages;
-    if (stages < 1) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (stages < min_stages) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (stages > P.max_stages) stages = P.max_stages > min_stages ? P.max_stages : min_stages;
 
     int64_t grid = (int64_t)sms * cps;
     if (grid > T) grid = T;

@@ -11,15 +11,16 @@
 // Main kernel: chunk c (= CTA c of a grid of n) owns the rows c, c + n, c + 2n, ...
 // (a static map, so the grid streams one window of consecutive rows at a time).  Its
 // producer thread streams the x and dy rows into a shared-memory ring; the consumer warps
-// read each row from its stage twice -- once to reduce sum((dy*w)*x) across the CTA,
-// once to write dx and add the row's dy*xhat into per-thread column accumulators that
-// stay in registers for the whole strip -- and then release the stage.  Each consumer
-// thread owns the same columns for every row; w is copied to shared memory once per CTA,
-// so the registers hold little besides the accumulators.  The accumulators
-// carry a compensated (high, low) pair:
-//   compensated = 1: every product is added with TwoSum;
-//   compensated = 0: the products of kBlockRows consecutive rows are summed with FMAs and
-//                    each block sum is added with TwoSum ("blocked FP32 sums").
+// take the rows in pairs and read each pair from its two stages twice -- once to reduce
+// sum((dy*w)*x) of both rows across the CTA (one barrier for the pair), once to write dx
+// and add dy*xhat into per-thread column accumulators that stay in registers for the whole
+// strip -- and then release both stages.  Each consumer thread owns the same columns for
+// every row and does a chunk of columns for both rows of a pair at once; w is copied to
+// shared memory (as FP32) once per CTA.  The accumulators carry a compensated (high, low)
+// pair:
+//   compensated = 1: every product is added with TwoSum, row by row;
+//   compensated = 0: the two products of a row pair are summed with one FMA and the block
+//                    sum is added with TwoSum ("blocked FP32 sums", blocks of two rows).
 // At the end of the strip the CTA writes its (high, low) partial row to the workspace
 // (deterministic mode) or adds high+low to dw with FP32 atomics.
 //
@@ -28,13 +29,13 @@
 // ranges), every step a TwoSum merge, rounded once at the end.  It is launched as a
 // programmatic dependent of the main kernel so its launch overlaps the main kernel's tail;
 // it waits for the main kernel's memory before reading the partials.
+#include <type_traits>
+
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
 
 namespace rmsn {
-
-constexpr int kBlockRows = 4;  // rows per FP32 block sum when compensated == 0
 
 struct BwdArgs {
     const void* dy;
@@ -95,90 +96,128 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     TX* __restrict__ DX = static_cast<TX*>(a.dx);
 
     constexpr int NP = Pairs<TX>::NP;
-    constexpr int NB = COMP ? 1 : NCH;  // block-sum registers (blocked mode only)
-    f2 hi[NCH][NP], lo[NCH][NP], blk[NB][NP];
+    f2 hi[NCH][NP], lo[NCH][NP];
 #pragma unroll
     for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int i = 0; i < NP; ++i) hi[c][i] = lo[c][i] = f2_splat(0.f);
-#pragma unroll
-    for (int c = 0; c < NB; ++c)
-#pragma unroll
-        for (int i = 0; i < NP; ++i) blk[c][i] = f2_splat(0.f);
 
-    int64_t k = 0;
-    for (; k < nrows; ++k) {
-        const int64_t row = b + k * nch;
-        const float rs = __ldg(a.rstd + row);
-        const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
-        const uint8_t* st = ring.stage((int)(k % ring.stages));
+    // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row
+    // may be alone, TWO = false).  Each chunk of columns is done for both rows at once, so
+    // one read of w from shared memory serves two rows.
 
-        // pass 1: sum_j (dy_j * w_j) * x_j over the row (x, dy read from the stage), in two
-        // chains (even and odd elements) added at the end
-        f2 dot2 = f2_splat(0.f);
+    // pass 1: d = sum_j (dy_j * w_j) * x_j per row (x, dy read from the stage), in two
+    // chains (even and odd elements) added at the end
+    auto pass1 = [&](auto two_tag, const uint8_t* s0, const uint8_t* s1, bool ok, float& d0,
+                     float& d1) {
+        constexpr bool TWO = decltype(two_tag)::value;
+        f2 acc0 = f2_splat(0.f), acc1 = f2_splat(0.f);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (ok && v < nvec) {
-                f2 xp[NP], dp[NP], wp[NP];
-                Pairs<TX>::get(lds128(st + (size_t)v * 16), xp);
-                Pairs<TX>::get(lds128(st + dy_off + (size_t)v * 16), dp);
+                f2 wp[NP], xp[NP], dp[NP];
                 w_pairs<NP>(wsm, nvec, v, wp);
+                Pairs<TX>::get(lds128(s0 + (size_t)v * 16), xp);
+                Pairs<TX>::get(lds128(s0 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
-                for (int i = 0; i < NP; ++i) dot2 = fma2(mul2(dp[i], wp[i]), xp[i], dot2);
+                for (int i = 0; i < NP; ++i) acc0 = fma2(mul2(dp[i], wp[i]), xp[i], acc0);
+                if constexpr (TWO) {
+                    Pairs<TX>::get(lds128(s1 + (size_t)v * 16), xp);
+                    Pairs<TX>::get(lds128(s1 + dy_off + (size_t)v * 16), dp);
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) acc1 = fma2(mul2(dp[i], wp[i]), xp[i], acc1);
+                }
             }
         }
-        float dot = __fadd_rn(f2_lo(dot2), f2_hi(dot2));
-        if (!consumer_sum(smem, dot, ok, nw, (int)(k & 1))) break;
-        // c = mean_j(g_j * xhat_j) = rstd * sum_j(g_j * x_j) / H
-        const float cm = __fdiv_rn(__fmul_rn(rs, dot), Hf);
-        const f2 rs2 = f2_splat(rs), ncm2 = f2_splat(-cm);
+        d0 = __fadd_rn(f2_lo(acc0), f2_hi(acc0));
+        d1 = TWO ? __fadd_rn(f2_lo(acc1), f2_hi(acc1)) : 0.f;
+    };
 
-        // pass 2: dx = rstd * (g - xhat * c) and the dw accumulators (x, dy read again)
+    // pass 2: dx = rstd * (g - xhat * c) with c = mean_j(g_j * xhat_j) = rstd * d / H
+    // (x, dy read again), and the dw accumulators:
+    //   compensated = 1: each product dy * xhat is added with TwoSum, row by row;
+    //   compensated = 0: the pair's block sum fma(dy1, xhat1, dy0 * xhat0) is added with
+    //                    TwoSum (a lone last row adds its own product).
+    auto pass2 = [&](auto two_tag, int64_t row0, const uint8_t* s0, const uint8_t* s1,
+                     float rs0, float rs1, float d0, float d1) {
+        constexpr bool TWO = decltype(two_tag)::value;
+        const float cm0 = __fdiv_rn(__fmul_rn(rs0, d0), Hf);
+        const float cm1 = TWO ? __fdiv_rn(__fmul_rn(rs1, d1), Hf) : 0.f;
+        const f2 rsa = f2_splat(rs0), ncma = f2_splat(-cm0);
+        const f2 rsb = f2_splat(rs1), ncmb = f2_splat(-cm1);
+        TX* dx0 = DX + row0 * H;
+        TX* dx1 = dx0 + nch * H;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (v < nvec) {
-                f2 xp[NP], dp[NP], wp[NP], o[NP];
-                Pairs<TX>::get(lds128(st + (size_t)v * 16), xp);
-                Pairs<TX>::get(lds128(st + dy_off + (size_t)v * 16), dp);
+                f2 wp[NP], xp[NP], dp[NP], o[NP], p0[NP];
                 w_pairs<NP>(wsm, nvec, v, wp);
+                Pairs<TX>::get(lds128(s0 + (size_t)v * 16), xp);
+                Pairs<TX>::get(lds128(s0 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
                 for (int i = 0; i < NP; ++i) {
-                    const f2 xh = mul2(xp[i], rs2);
-                    const f2 g = mul2(dp[i], wp[i]);
-                    o[i] = mul2(rs2, fma2(xh, ncm2, g));
-                    if constexpr (COMP) {
-                        comp_add2(hi[c][i], lo[c][i], mul2(dp[i], xh));
-                    } else {
-                        blk[c][i] = fma2(dp[i], xh, blk[c][i]);
-                    }
+                    const f2 xh = mul2(xp[i], rsa);
+                    o[i] = mul2(rsa, fma2(xh, ncma, mul2(dp[i], wp[i])));
+                    p0[i] = mul2(dp[i], xh);
                 }
-                st_stream(DX + row * H + (int64_t)v * VEC, Pairs<TX>::put(o));
-            }
-        }
-        ring_release(ring, k);  // every consumer warp has read the stage twice
-        if constexpr (!COMP) {
-            if ((k + 1) % kBlockRows == 0) {
-#pragma unroll
-                for (int c = 0; c < NCH; ++c)
+                st_stream(dx0 + (int64_t)v * VEC, Pairs<TX>::put(o));
+                if constexpr (TWO) {
+                    Pairs<TX>::get(lds128(s1 + (size_t)v * 16), xp);
+                    Pairs<TX>::get(lds128(s1 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
                     for (int i = 0; i < NP; ++i) {
-                        comp_add2(hi[c][i], lo[c][i], blk[c][i]);
-                        blk[c][i] = f2_splat(0.f);
+                        const f2 xh = mul2(xp[i], rsb);
+                        o[i] = mul2(rsb, fma2(xh, ncmb, mul2(dp[i], wp[i])));
+                        if constexpr (COMP) {
+                            comp_add2(hi[c][i], lo[c][i], p0[i]);
+                            comp_add2(hi[c][i], lo[c][i], mul2(dp[i], xh));
+                        } else {
+                            comp_add2(hi[c][i], lo[c][i], fma2(dp[i], xh, p0[i]));
+                        }
                     }
+                    st_stream(dx1 + (int64_t)v * VEC, Pairs<TX>::put(o));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) comp_add2(hi[c][i], lo[c][i], p0[i]);
+                }
             }
         }
+    };
+
+    int64_t k = 0;
+    int parity = 0;
+    Slot at0;
+    for (; k < nrows; k += 2, parity ^= 1) {
+        Slot at1 = at0;
+        at1.advance(ring.stages);
+        const uint8_t* s0 = ring.stage(at0.s);
+        const uint8_t* s1 = ring.stage(at1.s);
+        const int64_t row0 = b + k * nch;
+        float d0, d1;
+        if (k + 1 < nrows) {
+            const float rs0 = __ldg(a.rstd + row0);
+            const float rs1 = __ldg(a.rstd + row0 + nch);
+            const bool ok = ring_wait_full(ring, at0, a.limit_ns, a.err) &&
+                            ring_wait_full(ring, at1, a.limit_ns, a.err);
+            pass1(std::true_type{}, s0, s1, ok, d0, d1);
+            if (!consumer_sum2(smem, d0, d1, ok, nw, parity)) break;
+            pass2(std::true_type{}, row0, s0, s1, rs0, rs1, d0, d1);
+            ring_release(ring, at0);  // every consumer warp has read both stages twice
+            ring_release(ring, at1);
+        } else {
+            const float rs0 = __ldg(a.rstd + row0);
+            const bool ok = ring_wait_full(ring, at0, a.limit_ns, a.err);
+            pass1(std::false_type{}, s0, s1, ok, d0, d1);
+            if (!consumer_sum2(smem, d0, d1, ok, nw, parity)) break;
+            pass2(std::false_type{}, row0, s0, s1, rs0, 0.f, d0, 0.f);
+            ring_release(ring, at0);
+        }
+        at0 = at1;
+        at0.advance(ring.stages);
     }
     if (k < nrows) return;  // gave up (error word set): leave the outputs as they are
-    if constexpr (!COMP) {
-        if (nrows % kBlockRows != 0) {
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) comp_add2(hi[c][i], lo[c][i], blk[c][i]);
-        }
-    }
 
     // ---- emit the chunk's partial (pairs are consecutive columns)
 #pragma unroll

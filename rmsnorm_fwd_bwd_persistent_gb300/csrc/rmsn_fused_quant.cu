@@ -106,11 +106,12 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
     const float Hf = (float)H;
     constexpr int NP = 4;  // FP32 pairs per 16-byte vector of bf16
 
-    for (int64_t k = 0; k < nrows; ++k) {
+    Slot at;
+    for (int64_t k = 0; k < nrows; ++k, at.advance(ring.stages)) {
         const int64_t row = b + k * G;
         const int64_t base = row * H;
-        const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
-        const uint8_t* st = ring.stage((int)(k % ring.stages));
+        const bool ok = ring_wait_full(ring, at, a.limit_ns, a.err);
+        const uint8_t* st = ring.stage(at.s);
         uint4 hv[NCH];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
             for (int i = 0; i < NP; ++i) rp[i] = add2(xp[i], rp[i]);
             hv[c] = Pairs<__nv_bfloat16>::put(rp);  // h rounded once to bf16
         }
-        if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
+        if (__all_sync(0xffffffffu, ok)) ring_release(ring, at);
         f2 ss2 = f2_splat(0.f);  // even and odd elements, added at the end
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {

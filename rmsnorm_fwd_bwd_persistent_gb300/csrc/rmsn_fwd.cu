@@ -66,17 +66,18 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
     const float Hf = (float)a.H;
     TX* __restrict__ Y = static_cast<TX*>(a.y);
 
-    for (int64_t k = 0; k < nrows; ++k) {
+    Slot at;
+    for (int64_t k = 0; k < nrows; ++k, at.advance(ring.stages)) {
         const int64_t row = b + k * G;
-        const bool ok = ring_wait_full(ring, k, a.limit_ns, a.err);
-        const uint8_t* st = ring.stage((int)(k % ring.stages));
+        const bool ok = ring_wait_full(ring, at, a.limit_ns, a.err);
+        const uint8_t* st = ring.stage(at.s);
         uint4 xv[NCH];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             xv[c] = (ok && v < nvec) ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
         }
-        if (__all_sync(0xffffffffu, ok)) ring_release(ring, k);
+        if (__all_sync(0xffffffffu, ok)) ring_release(ring, at);
 
         // sum of squares in two chains (even and odd elements), one pair instruction per two
         // elements; the chains are added at the end (a fixed order, same on every run)

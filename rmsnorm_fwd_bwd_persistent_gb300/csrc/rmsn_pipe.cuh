@@ -138,9 +138,27 @@ struct Ring {
     __device__ __forceinline__ uint8_t* stage(int s) const { return data + (size_t)s * stage_bytes; }
 };
 
-// Dynamic shared memory layout: [full[S] | empty[S] | reduce slots (2 x 32 floats) |
-// abort flags (2 x 32 ints)] (kRingHeader bytes) [weights, padded to 128] [S stages].
-constexpr int kRingHeader = 1024;  // bytes reserved before the weights (S <= 32)
+// Position of the k-th row in the ring: stage s = k mod S and the parity ph = (k div S) mod 2
+// of that stage's current phase, advanced row by row (no division in the row loops).
+struct Slot {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void advance(int stages) {
+        if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Dynamic shared memory layout (kRingHeader bytes of bookkeeping, then the weights padded
+// to 128 bytes, then the stages):
+//   [0, 256)      full[32]      mbarriers, one per stage
+//   [256, 512)    empty[32]     mbarriers, one per stage
+//   [512, 768)    red[2][32]    per-warp partial sums (one value per row)
+//   [768, 832)    abort[2][32]  per-warp "gave up" flags, one byte each
+//   [1024, 1536)  red2[2][32]   per-warp partial sums (two values, two rows at a time)
+constexpr int kRingHeader = 2048;  // bytes reserved before the weights (S <= 32)
 
 __device__ __forceinline__ Ring ring_at(uint8_t* smem, int stages, uint32_t stage_bytes,
                                         uint32_t data_offset) {
@@ -156,8 +174,11 @@ __device__ __forceinline__ Ring ring_at(uint8_t* smem, int stages, uint32_t stag
 __device__ __forceinline__ float* ring_red(uint8_t* smem) {
     return reinterpret_cast<float*>(smem + 512);  // [2][32] per-warp partial sums
 }
-__device__ __forceinline__ int* ring_abort(uint8_t* smem) {
-    return reinterpret_cast<int*>(smem + 768);    // [2][32] per-warp "gave up" flags
+__device__ __forceinline__ uint8_t* ring_abort(uint8_t* smem) {
+    return smem + 768;                              // [2][32] per-warp "gave up" bytes
+}
+__device__ __forceinline__ float2* ring_red2(uint8_t* smem) {
+    return reinterpret_cast<float2*>(smem + 1024);  // [2][32] per-warp partial sum pairs
 }
 
 // Initializes the barriers (thread 0) and makes them visible to the CTA.
@@ -179,16 +200,14 @@ template <typename Issue>
 __device__ __forceinline__ int64_t ring_produce(const Ring& r, int64_t nrows, uint64_t limit_ns,
                                                 unsigned* err, Issue issue) {
     int64_t k = 0;
-    for (; k < nrows; ++k) {
-        const int s = (int)(k % r.stages);
-        if (k >= r.stages) {
-            const uint32_t par = (uint32_t)(((k / r.stages) & 1) ^ 1);
-            if (!mbar_wait(&r.empty[s], par, limit_ns)) {
-                atomicOr(err, ERR_WAIT_EMPTY);
-                break;
-            }
+    Slot at;
+    for (; k < nrows; ++k, at.advance(r.stages)) {
+        // a stage is refilled once every consumer warp has released its previous row
+        if (k >= r.stages && !mbar_wait(&r.empty[at.s], at.ph ^ 1u, limit_ns)) {
+            atomicOr(err, ERR_WAIT_EMPTY);
+            break;
         }
-        issue(k, r.stage(s), &r.full[s]);
+        issue(k, r.stage(at.s), &r.full[at.s]);
     }
     return k;
 }
@@ -207,36 +226,56 @@ __device__ __forceinline__ void ring_drain(const Ring& r, int64_t issued, uint64
     }
 }
 
-// Consumer side: wait for row k's stage.  The decision to go on is taken together by
-// all consumer warps at the next named barrier (see consumer_sync), so a warp that gave
-// up never leaves the others waiting at a barrier.
-__device__ __forceinline__ bool ring_wait_full(const Ring& r, int64_t k, uint64_t limit_ns,
+// Consumer side: wait for the row in stage `at`.  The decision to go on is taken together
+// by all consumer warps at the next named barrier (consumer_sum), so a warp that gave up
+// never leaves the others waiting at a barrier.
+__device__ __forceinline__ bool ring_wait_full(const Ring& r, const Slot& at, uint64_t limit_ns,
                                                unsigned* err) {
-    const int s = (int)(k % r.stages);
-    if (mbar_wait(&r.full[s], (uint32_t)((k / r.stages) & 1), limit_ns)) return true;
+    if (mbar_wait(&r.full[at.s], at.ph, limit_ns)) return true;
     atomicOr(err, ERR_WAIT_FULL);
     return false;
 }
 
-__device__ __forceinline__ void ring_release(const Ring& r, int64_t k) {
+__device__ __forceinline__ void ring_release(const Ring& r, const Slot& at) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[(int)(k % r.stages)]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[at.s]);
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// True if any of the first nw (1, 2, 4 or 8) "gave up" bytes at f (8-byte aligned) is set.
+__device__ __forceinline__ bool any_gave_up(const uint8_t* f, int nw) {
+    const uint64_t all = *reinterpret_cast<const uint64_t*>(f);
+    const uint64_t mask = nw >= 8 ? ~0ull : ((1ull << (8 * nw)) - 1ull);
+    return (all & mask) != 0;
+}
+
+// r[0] + r[1] + ... + r[nw-1], left to right, for nw in {1, 2, 4, 8} (r 16-byte aligned).
+__device__ __forceinline__ float sum_posts(const float* r, int nw) {
+    if (nw >= 4) {
+        const float4 a = *reinterpret_cast<const float4*>(r);
+        float s = a.x + a.y + a.z + a.w;
+        if (nw == 8) {
+            const float4 b = *reinterpret_cast<const float4*>(r + 4);
+            s = s + b.x + b.y + b.z + b.w;
+        }
+        return s;
+    }
+    return nw == 2 ? r[0] + r[1] : r[0];
+}
+
 // Row-wide sum over the consumer warps (warps 0 .. nw-1), combined with the "keep going"
-// vote: every consumer warp posts its warp sum and whether its wait succeeded, one named
-// barrier, then every lane adds the posts in warp order (same bits on every lane).
-// Returns false if any consumer warp gave up on this row.
+// vote: every consumer warp reduces its value by a butterfly of shuffles and posts it with
+// whether its wait succeeded, one named barrier, then every lane adds the posts in warp
+// order (same bits on every lane).  Returns false if any consumer warp gave up on this row.
 __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, int nw,
                                              int parity) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     float* red = ring_red(smem) + parity * 32;
-    int* ab = ring_abort(smem) + parity * 32;
+    uint8_t* ab = ring_abort(smem) + parity * 32;
     const int warp = threadIdx.x >> 5;
     const bool warp_ok = __all_sync(0xffffffffu, ok);
     if ((threadIdx.x & 31) == 0) {
@@ -244,14 +283,46 @@ __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, i
         ab[warp] = warp_ok ? 0 : 1;
     }
     named_bar(1, nw * 32);
-    float s = red[0];
-    int bad = ab[0];
-    for (int k = 1; k < nw; ++k) {
-        s += red[k];
-        bad |= ab[k];
+    v = sum_posts(red, nw);
+    return !any_gave_up(ab, nw);
+}
+
+// Two row-wide sums at once (two rows share one barrier).  The first shuffle pairs the
+// lanes so that even lanes go on with v0 and odd lanes with v1; four more butterfly levels
+// among lanes of the same parity finish both warp sums (lane 0 holds v0's, lane 1 v1's).
+// The posts are then added in warp order.  The order is fixed, so the bits depend only on
+// the data.
+__device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v1, bool ok,
+                                              int nw, int parity) {
+    const int lane = threadIdx.x & 31;
+    const bool odd = (lane & 1) != 0;
+    float mine = odd ? v1 : v0;
+    mine += __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+#pragma unroll
+    for (int o = 16; o > 1; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    float* red = reinterpret_cast<float*>(ring_red2(smem) + parity * 32);
+    uint8_t* ab = ring_abort(smem) + parity * 32;
+    const int warp = threadIdx.x >> 5;
+    const bool warp_ok = __all_sync(0xffffffffu, ok);
+    if (lane < 2) red[2 * warp + lane] = mine;
+    if (lane == 0) ab[warp] = warp_ok ? 0 : 1;
+    named_bar(1, nw * 32);
+    const float4* r4 = reinterpret_cast<const float4*>(red);
+    if (nw == 1) {
+        v0 = red[0];
+        v1 = red[1];
+    } else {
+        float4 q = r4[0];
+        float s0 = q.x + q.z, s1 = q.y + q.w;
+        for (int j = 1; j < nw / 2; ++j) {
+            q = r4[j];
+            s0 = s0 + q.x + q.z;
+            s1 = s1 + q.y + q.w;
+        }
+        v0 = s0;
+        v1 = s1;
     }
-    v = s;
-    return bad == 0;
+    return !any_gave_up(ab, nw);
 }
 
 }  // namespace rmsn
