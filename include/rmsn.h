@@ -207,7 +207,8 @@ typedef struct {
     int vec_elems;        /* elements per 16-byte vector */
     int consumer_warps;   /* warps that share one row */
     int chunks_per_lane;  /* 16-byte vectors each consumer lane holds per row */
-    int threads;          /* threads per CTA (consumer warps + one producer warp) */
+    int threads;          /* threads per CTA: the consumer warps, plus one producer warp
+                             in the forward and fused kernels */
     int stages;           /* depth of the shared-memory row ring */
     int ctas_per_sm;      /* CTAs per SM the grid is sized for */
     int64_t grid;         /* CTAs launched (for the backward: the number of row chunks) */

@@ -283,7 +283,7 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
     out->vec_elems = 16 / esize(x_dtype);
     out->consumer_warps = L.nw;
     out->chunks_per_lane = L.nch;
-    out->threads = L.nw * 32 + 32;
+    out->threads = (op == RMSN_OP_BWD) ? L.nw * 32 : L.nw * 32 + 32;  // bwd: no producer warp
     out->stages = L.stages;
     out->ctas_per_sm = L.ctas_per_sm;
     out->grid = L.grid;

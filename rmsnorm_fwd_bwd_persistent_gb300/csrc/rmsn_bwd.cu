@@ -9,17 +9,19 @@
 // blocked FP32 weight-gradient sums (#8848).
 //
 // Main kernel: chunk c (= CTA c of a grid of n) owns the rows c, c + n, c + 2n, ...
-// (a static map, so the grid streams one window of consecutive rows at a time).  Its
-// producer thread streams the x and dy rows into a shared-memory ring; the consumer warps
-// take the rows in pairs and read each pair from its two stages twice -- once to reduce
-// sum((dy*w)*x) of both rows across the CTA (one barrier for the pair), once to write dx
-// and add dy*xhat into per-thread column accumulators that stay in registers for the whole
-// strip -- and then release both stages.  Each consumer thread owns the same columns for
-// every row and does a chunk of columns for both rows of a pair at once; w is copied to
-// shared memory (as FP32) once per CTA.  The accumulators carry a compensated (high, low)
-// pair:
-//   compensated = 1: every product is added with TwoSum, row by row;
-//   compensated = 0: the two products of a row pair are summed with one FMA and the block
+// (a static map, so the grid streams one window of consecutive rows at a time).  Consumer
+// thread 0 streams the x and dy rows into a shared-memory ring (there is no producer warp,
+// so each thread may hold more registers).  The consumer warps take the rows in pairs.
+// Pass 1 reads a pair from its two stages and forms p = dy * x per element (exact for bf16
+// inputs, one mixed-precision FMA each), the rows' d = sum(w * p), and adds the dw terms
+// dy * xhat = rstd * p into per-thread column accumulators that stay in registers for the
+// whole strip.  One barrier carries both rows' d across the CTA (already scaled to
+// c' = rstd^2 * d / H); pass 2 writes dx = rstd * (dy * w - c' * x).  Each consumer thread
+// owns the same columns for every row and does a chunk of columns for both rows of a pair
+// at once; w is copied to shared memory (as FP32) once per CTA.  The accumulators carry a
+// compensated (high, low) pair:
+//   compensated = 1: every term is added with TwoSum, row by row;
+//   compensated = 0: the two terms of a row pair are summed with one FMA and the block
 //                    sum is added with TwoSum ("blocked FP32 sums", blocks of two rows).
 // At the end of the strip the CTA writes its (high, low) partial row to the workspace
 // (deterministic mode) or adds high+low to dw with FP32 atomics.
@@ -59,7 +61,7 @@ struct BwdArgs {
 };
 
 template <typename TX, typename TW, int NCH, bool COMP>
-__global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
     const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);
@@ -72,27 +74,44 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     stage_weights_f32<VEC>(static_cast<const TW*>(a.w), a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
-    if ((int)(threadIdx.x >> 5) == nw) {  // producer warp
-        if ((threadIdx.x & 31) == 0) {
-            const uint8_t* X = static_cast<const uint8_t*>(a.x);
-            const uint8_t* DY = static_cast<const uint8_t*>(a.dy);
-            const int64_t issued = ring_produce(
-                ring, nrows, a.limit_ns, a.err, [&](int64_t k, uint8_t* dst, uint64_t* full) {
-                    const int64_t off = (b + k * nch) * (int64_t)a.row_bytes;
-                    mbar_arrive_expect_tx(full, 2 * a.row_bytes);
-                    bulk_load(dst, X + off, a.row_bytes, full);
-                    bulk_load(dst + dy_off, DY + off, a.row_bytes, full);
-                });
-            ring_drain(ring, issued, a.limit_ns, a.err);
+    // Let the column-reduce grid launch as soon as CTAs of this grid finish; it waits
+    // (griddepcontrol.wait) for this whole grid and its memory before reading the partials.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // Thread 0 feeds the ring (there is no producer warp): it issues the copies of the
+    // CTA's rows in order, row r into stage r mod S once every consumer warp has released
+    // row r - S (empty barrier).  Each pair's barrier (consumer_sum2) shows that all warps
+    // are done with the rows before the pair, so right after it those stages are refilled
+    // without waiting; before a pair's rows are waited for, any of them not yet issued (a
+    // ring shallower than two pairs) is issued, waiting for its stage.
+    const uint8_t* X = static_cast<const uint8_t*>(a.x);
+    const uint8_t* DY = static_cast<const uint8_t*>(a.dy);
+    int64_t issued = 0;   // rows issued so far (thread 0)
+    Slot in;              // stage of row `issued`
+    bool feed_ok = true;  // false once a wait for a free stage ran out
+    auto issue_below = [&](int64_t lim) {
+        if (threadIdx.x != 0 || !feed_ok) return;
+        const int64_t end = lim < nrows ? lim : nrows;
+        for (; issued < end; ++issued, in.advance(ring.stages)) {
+            if (issued >= ring.stages && !mbar_wait(&ring.empty[in.s], in.ph ^ 1u, a.limit_ns)) {
+                atomicOr(a.err, ERR_WAIT_EMPTY);
+                feed_ok = false;
+                return;
+            }
+            const int64_t off = (b + issued * nch) * (int64_t)a.row_bytes;
+            uint8_t* dst = ring.stage(in.s);
+            mbar_arrive_expect_tx(&ring.full[in.s], 2 * a.row_bytes);
+            bulk_load(dst, X + off, a.row_bytes, &ring.full[in.s]);
+            bulk_load(dst + dy_off, DY + off, a.row_bytes, &ring.full[in.s]);
         }
-        return;
-    }
+    };
+    issue_below(ring.stages);
 
     const int t = threadIdx.x;
     const int NC = nw * 32;
     const int H = a.H;
     const int nvec = H / VEC;
-    const float Hf = (float)H;
+    const float invH = __frcp_rn((float)H);  // 1/H rounded once
     TX* __restrict__ DX = static_cast<TX*>(a.dx);
 
     constexpr int NP = Pairs<TX>::NP;
@@ -102,31 +121,58 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < NP; ++i) hi[c][i] = lo[c][i] = f2_splat(0.f);
 
+    // KEEP: pass 1 keeps the pair's x and dy vectors in registers for pass 2, so both
+    // stages are released before the barrier and the whole ring can be in flight during
+    // pass 2.  Otherwise (long rows) pass 2 reads them from the stages again.
+    constexpr bool KEEP = NCH <= 2;
+    uint4 xr[2][NCH], dr[2][NCH];
+
     // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row
     // may be alone, TWO = false).  Each chunk of columns is done for both rows at once, so
     // one read of w from shared memory serves two rows.
 
-    // pass 1: d = sum_j (dy_j * w_j) * x_j per row (x, dy read from the stage), in two
-    // chains (even and odd elements) added at the end
-    auto pass1 = [&](auto two_tag, const uint8_t* s0, const uint8_t* s1, bool ok, float& d0,
-                     float& d1) {
+    // pass 1 (before the pair's barrier): per row, the products p_j = dy_j * x_j (exact
+    // for bf16 inputs), the row's d = sum_j w_j * p_j in two chains (even and odd elements)
+    // added at the end, and the dw terms dy_j * xhat_j = rstd * p_j into the accumulators:
+    //   compensated = 1: each term is added with TwoSum, row by row;
+    //   compensated = 0: the pair's block sum fma(rstd1, p1_j, rstd0 * p0_j) is added with
+    //                    TwoSum (a lone last row adds its own term).
+    auto pass1 = [&](auto two_tag, const uint8_t* s0, const uint8_t* s1, bool ok, float rs0,
+                     float rs1, float& d0, float& d1) {
         constexpr bool TWO = decltype(two_tag)::value;
+        const f2 rsa = f2_splat(rs0), rsb = f2_splat(rs1);
         f2 acc0 = f2_splat(0.f), acc1 = f2_splat(0.f);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (ok && v < nvec) {
-                f2 wp[NP], xp[NP], dp[NP];
+                f2 wp[NP], p[NP], q0[NP];
                 w_pairs<NP>(wsm, nvec, v, wp);
-                Pairs<TX>::get(lds128(s0 + (size_t)v * 16), xp);
-                Pairs<TX>::get(lds128(s0 + dy_off + (size_t)v * 16), dp);
+                xr[0][c] = lds128(s0 + (size_t)v * 16);
+                dr[0][c] = lds128(s0 + dy_off + (size_t)v * 16);
+                Pairs<TX>::prod(dr[0][c], xr[0][c], p);
 #pragma unroll
-                for (int i = 0; i < NP; ++i) acc0 = fma2(mul2(dp[i], wp[i]), xp[i], acc0);
+                for (int i = 0; i < NP; ++i) {
+                    acc0 = fma2(wp[i], p[i], acc0);
+                    q0[i] = mul2(rsa, p[i]);
+                }
                 if constexpr (TWO) {
-                    Pairs<TX>::get(lds128(s1 + (size_t)v * 16), xp);
-                    Pairs<TX>::get(lds128(s1 + dy_off + (size_t)v * 16), dp);
+                    xr[1][c] = lds128(s1 + (size_t)v * 16);
+                    dr[1][c] = lds128(s1 + dy_off + (size_t)v * 16);
+                    Pairs<TX>::prod(dr[1][c], xr[1][c], p);
 #pragma unroll
-                    for (int i = 0; i < NP; ++i) acc1 = fma2(mul2(dp[i], wp[i]), xp[i], acc1);
+                    for (int i = 0; i < NP; ++i) {
+                        acc1 = fma2(wp[i], p[i], acc1);
+                        if constexpr (COMP) {
+                            comp_add2(hi[c][i], lo[c][i], q0[i]);
+                            comp_add2(hi[c][i], lo[c][i], mul2(rsb, p[i]));
+                        } else {
+                            comp_add2(hi[c][i], lo[c][i], fma2(rsb, p[i], q0[i]));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) comp_add2(hi[c][i], lo[c][i], q0[i]);
                 }
             }
         }
@@ -134,53 +180,33 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
         d1 = TWO ? __fadd_rn(f2_lo(acc1), f2_hi(acc1)) : 0.f;
     };
 
-    // pass 2: dx = rstd * (g - xhat * c) with c = mean_j(g_j * xhat_j) = rstd * d / H
-    // (x, dy read again), and the dw accumulators:
-    //   compensated = 1: each product dy * xhat is added with TwoSum, row by row;
-    //   compensated = 0: the pair's block sum fma(dy1, xhat1, dy0 * xhat0) is added with
-    //                    TwoSum (a lone last row adds its own product).
+    // pass 2 (after the barrier): dx = rstd * (g - c' * x) with g = dy * w and
+    // c' = rstd * c, c = mean_j(g_j * xhat_j) = rstd * d / H; the barrier hands over c'
+    // (x, dy from the registers or read again)
     auto pass2 = [&](auto two_tag, int64_t row0, const uint8_t* s0, const uint8_t* s1,
-                     float rs0, float rs1, float d0, float d1) {
+                     float rs0, float rs1, float c0, float c1) {
         constexpr bool TWO = decltype(two_tag)::value;
-        const float cm0 = __fdiv_rn(__fmul_rn(rs0, d0), Hf);
-        const float cm1 = TWO ? __fdiv_rn(__fmul_rn(rs1, d1), Hf) : 0.f;
-        const f2 rsa = f2_splat(rs0), ncma = f2_splat(-cm0);
-        const f2 rsb = f2_splat(rs1), ncmb = f2_splat(-cm1);
+        const f2 rsa = f2_splat(rs0), nca = f2_splat(-c0);
+        const f2 rsb = f2_splat(rs1), ncb = f2_splat(-c1);
         TX* dx0 = DX + row0 * H;
         TX* dx1 = dx0 + nch * H;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             if (v < nvec) {
-                f2 wp[NP], xp[NP], dp[NP], o[NP], p0[NP];
+                f2 wp[NP], xp[NP], dp[NP], o[NP];
                 w_pairs<NP>(wsm, nvec, v, wp);
-                Pairs<TX>::get(lds128(s0 + (size_t)v * 16), xp);
-                Pairs<TX>::get(lds128(s0 + dy_off + (size_t)v * 16), dp);
+                Pairs<TX>::get(KEEP ? xr[0][c] : lds128(s0 + (size_t)v * 16), xp);
+                Pairs<TX>::get(KEEP ? dr[0][c] : lds128(s0 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const f2 xh = mul2(xp[i], rsa);
-                    o[i] = mul2(rsa, fma2(xh, ncma, mul2(dp[i], wp[i])));
-                    p0[i] = mul2(dp[i], xh);
-                }
+                for (int i = 0; i < NP; ++i) o[i] = mul2(rsa, fma2(xp[i], nca, mul2(dp[i], wp[i])));
                 st_stream(dx0 + (int64_t)v * VEC, Pairs<TX>::put(o));
                 if constexpr (TWO) {
-                    Pairs<TX>::get(lds128(s1 + (size_t)v * 16), xp);
-                    Pairs<TX>::get(lds128(s1 + dy_off + (size_t)v * 16), dp);
+                    Pairs<TX>::get(KEEP ? xr[1][c] : lds128(s1 + (size_t)v * 16), xp);
+                    Pairs<TX>::get(KEEP ? dr[1][c] : lds128(s1 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        const f2 xh = mul2(xp[i], rsb);
-                        o[i] = mul2(rsb, fma2(xh, ncmb, mul2(dp[i], wp[i])));
-                        if constexpr (COMP) {
-                            comp_add2(hi[c][i], lo[c][i], p0[i]);
-                            comp_add2(hi[c][i], lo[c][i], mul2(dp[i], xh));
-                        } else {
-                            comp_add2(hi[c][i], lo[c][i], fma2(dp[i], xh, p0[i]));
-                        }
-                    }
+                    for (int i = 0; i < NP; ++i) o[i] = mul2(rsb, fma2(xp[i], ncb, mul2(dp[i], wp[i])));
                     st_stream(dx1 + (int64_t)v * VEC, Pairs<TX>::put(o));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) comp_add2(hi[c][i], lo[c][i], p0[i]);
                 }
             }
         }
@@ -189,35 +215,64 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     int64_t k = 0;
     int parity = 0;
     Slot at0;
+    // rstd of the next pair, loaded one pair ahead
+    float rs_n0 = nrows > 0 ? __ldg(a.rstd + b) : 0.f;
+    float rs_n1 = nrows > 1 ? __ldg(a.rstd + b + nch) : 0.f;
     for (; k < nrows; k += 2, parity ^= 1) {
         Slot at1 = at0;
         at1.advance(ring.stages);
         const uint8_t* s0 = ring.stage(at0.s);
         const uint8_t* s1 = ring.stage(at1.s);
         const int64_t row0 = b + k * nch;
+        const float rs0 = rs_n0, rs1 = rs_n1;
+        if (k + 2 < nrows) rs_n0 = __ldg(a.rstd + row0 + 2 * nch);
+        if (k + 3 < nrows) rs_n1 = __ldg(a.rstd + row0 + 3 * nch);
         float d0, d1;
+        issue_below(k + 2);
         if (k + 1 < nrows) {
-            const float rs0 = __ldg(a.rstd + row0);
-            const float rs1 = __ldg(a.rstd + row0 + nch);
             const bool ok = ring_wait_full(ring, at0, a.limit_ns, a.err) &&
                             ring_wait_full(ring, at1, a.limit_ns, a.err);
-            pass1(std::true_type{}, s0, s1, ok, d0, d1);
-            if (!consumer_sum2(smem, d0, d1, ok, nw, parity)) break;
+            pass1(std::true_type{}, s0, s1, ok, rs0, rs1, d0, d1);
+            if (KEEP && ok) {  // this warp is done with both stages
+                ring_release(ring, at0);
+                ring_release(ring, at1);
+            }
+            // c' = rstd^2 * d / H: each warp's part of d is scaled by rstd^2 / H before the
+            // parts are added
+            if (!consumer_sum2(smem, d0, d1, __fmul_rn(rs0, __fmul_rn(rs0, invH)),
+                               __fmul_rn(rs1, __fmul_rn(rs1, invH)), ok, nw, parity))
+                break;
+            // every warp is done with the rows before the pair (and with the pair if KEEP)
+            issue_below(k + (KEEP ? 2 : 0) + ring.stages);
             pass2(std::true_type{}, row0, s0, s1, rs0, rs1, d0, d1);
-            ring_release(ring, at0);  // every consumer warp has read both stages twice
-            ring_release(ring, at1);
+            if (!KEEP) {  // this warp has read both stages twice
+                ring_release(ring, at0);
+                ring_release(ring, at1);
+            }
         } else {
-            const float rs0 = __ldg(a.rstd + row0);
             const bool ok = ring_wait_full(ring, at0, a.limit_ns, a.err);
-            pass1(std::false_type{}, s0, s1, ok, d0, d1);
-            if (!consumer_sum2(smem, d0, d1, ok, nw, parity)) break;
+            pass1(std::false_type{}, s0, s1, ok, rs0, 0.f, d0, d1);
+            if (!consumer_sum2(smem, d0, d1, __fmul_rn(rs0, __fmul_rn(rs0, invH)), 0.f, ok, nw,
+                               parity))
+                break;
             pass2(std::false_type{}, row0, s0, s1, rs0, 0.f, d0, 0.f);
-            ring_release(ring, at0);
         }
         at0 = at1;
         at0.advance(ring.stages);
     }
-    if (k < nrows) return;  // gave up (error word set): leave the outputs as they are
+    if (k < nrows) {
+        // gave up (error word set): leave the outputs as they are, but let every copy
+        // still in flight land before the CTA exits
+        if (threadIdx.x == 0) {
+            for (int64_t r = k; r < issued; ++r, at0.advance(ring.stages)) {
+                if (!mbar_wait(&ring.full[at0.s], at0.ph, a.limit_ns)) {
+                    atomicOr(a.err, ERR_WAIT_DRAIN);
+                    break;
+                }
+            }
+        }
+        return;
+    }
 
     // ---- emit the chunk's partial (pairs are consecutive columns)
 #pragma unroll
@@ -243,8 +298,6 @@ __global__ void __launch_bounds__(288, 2) rmsnorm_bwd_kernel(BwdArgs a) {
             }
         }
     }
-    // Let the column-reduce grid start launching; it still waits for this grid's memory.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // dw[j] = fixed-order compensated sum over the chunk partials.  A CTA covers 16 columns
@@ -317,7 +370,7 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce_kernel(const float* __r
 template <typename TX, typename TW, int NCH, bool COMP>
 static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s, int64_t* grid) {
     auto k = rmsnorm_bwd_kernel<TX, TW, NCH, COMP>;
-    const int threads = L.nw * 32 + 32;
+    const int threads = L.nw * 32;  // consumer warps only
     cudaError_t e = fit_grid((const void*)k, L, threads, grid);
     if (e != cudaSuccess) return e;
     k<<<(unsigned)*grid, threads, (size_t)L.smem, s>>>(a);

@@ -123,6 +123,14 @@ struct Pairs<float> {
         return make_uint4(__float_as_uint(f2_lo(p[0])), __float_as_uint(f2_hi(p[0])),
                           __float_as_uint(f2_lo(p[1])), __float_as_uint(f2_hi(p[1])));
     }
+    // elementwise products a * b, rounded to FP32
+    __device__ __forceinline__ static void prod(const uint4& a, const uint4& b, f2 (&p)[2]) {
+        f2 x[2], y[2];
+        get(a, x);
+        get(b, y);
+        p[0] = mul2(x[0], y[0]);
+        p[1] = mul2(x[1], y[1]);
+    }
 };
 
 template <>
@@ -140,6 +148,26 @@ struct Pairs<__nv_bfloat16> {
     }
     __device__ __forceinline__ static uint4 put(const f2 (&p)[4]) {
         return make_uint4(round_word(p[0]), round_word(p[1]), round_word(p[2]), round_word(p[3]));
+    }
+    // Elementwise products of two words of bf16 pairs, each by one mixed-precision FMA
+    // (bf16 operands, FP32 addend +0 and result).  A product of two bf16 values has at most
+    // 16 significant bits, so it is exact in FP32 unless it leaves FP32's normal range.
+    __device__ __forceinline__ static f2 word_prod(uint32_t a, uint32_t b) {
+        float lo, hi;
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+            "mov.b32 {a0, a1}, %2;\n\t"
+            "mov.b32 {b0, b1}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, 0f00000000;\n\t"
+            "fma.rn.f32.bf16 %1, a1, b1, 0f00000000;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(a), "r"(b));
+        return f2_make(lo, hi);
+    }
+    __device__ __forceinline__ static void prod(const uint4& a, const uint4& b, f2 (&p)[4]) {
+        p[0] = word_prod(a.x, b.x);
+        p[1] = word_prod(a.y, b.y);
+        p[2] = word_prod(a.z, b.z);
+        p[3] = word_prod(a.w, b.w);
     }
 };
 

@@ -290,10 +290,10 @@ __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, i
 // Two row-wide sums at once (two rows share one barrier).  The first shuffle pairs the
 // lanes so that even lanes go on with v0 and odd lanes with v1; four more butterfly levels
 // among lanes of the same parity finish both warp sums (lane 0 holds v0's, lane 1 v1's).
-// The posts are then added in warp order.  The order is fixed, so the bits depend only on
-// the data.
-__device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v1, bool ok,
-                                              int nw, int parity) {
+// Each warp posts its sums times m0 and m1 (rounded), and the posts are added in warp
+// order.  The order is fixed, so the bits depend only on the data.  nw is 1, 2, 4 or 8.
+__device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v1, float m0,
+                                              float m1, bool ok, int nw, int parity) {
     const int lane = threadIdx.x & 31;
     const bool odd = (lane & 1) != 0;
     float mine = odd ? v1 : v0;
@@ -304,24 +304,29 @@ __device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v
     uint8_t* ab = ring_abort(smem) + parity * 32;
     const int warp = threadIdx.x >> 5;
     const bool warp_ok = __all_sync(0xffffffffu, ok);
-    if (lane < 2) red[2 * warp + lane] = mine;
+    if (lane < 2) red[2 * warp + lane] = __fmul_rn(mine, odd ? m1 : m0);
     if (lane == 0) ab[warp] = warp_ok ? 0 : 1;
     named_bar(1, nw * 32);
     const float4* r4 = reinterpret_cast<const float4*>(red);
-    if (nw == 1) {
-        v0 = red[0];
-        v1 = red[1];
+    float s0, s1;
+    if (nw == 8) {
+        const float4 a = r4[0], b = r4[1], c = r4[2], d = r4[3];
+        s0 = a.x + a.z + b.x + b.z + c.x + c.z + d.x + d.z;
+        s1 = a.y + a.w + b.y + b.w + c.y + c.w + d.y + d.w;
+    } else if (nw == 4) {
+        const float4 a = r4[0], b = r4[1];
+        s0 = a.x + a.z + b.x + b.z;
+        s1 = a.y + a.w + b.y + b.w;
+    } else if (nw == 2) {
+        const float4 a = r4[0];
+        s0 = a.x + a.z;
+        s1 = a.y + a.w;
     } else {
-        float4 q = r4[0];
-        float s0 = q.x + q.z, s1 = q.y + q.w;
-        for (int j = 1; j < nw / 2; ++j) {
-            q = r4[j];
-            s0 = s0 + q.x + q.z;
-            s1 = s1 + q.y + q.w;
-        }
-        v0 = s0;
-        v1 = s1;
+        s0 = red[0];
+        s1 = red[1];
     }
+    v0 = s0;
+    v1 = s1;
     return !any_gave_up(ab, nw);
 }
 

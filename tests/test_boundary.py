@@ -112,7 +112,8 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         lanes = 32 * p["consumer_warps"]
         assert p["vec_elems"] == vec
         assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
-        assert p["threads"] == lanes + 32 and p["threads"] <= 288   # + one producer warp
+        producer = 0 if op == rmsn.OP_BWD else 32                   # bwd: thread 0 feeds the ring
+        assert p["threads"] == lanes + producer and p["threads"] <= 288
         assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
         row = H * (2 if xd == 1 else 4)
         stage = -(-row // 128) * 128 * (1 if op == rmsn.OP_FWD else 2)
