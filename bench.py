@@ -41,7 +41,6 @@ WORKLOAD = ("RMSNorm forward + fused dX/dW backward (deterministic) + fused resi
             "RMSNorm/E4M3 1x128 block quant, T=8192 H=4096 bf16 (fp32 rstd, dW, scales)")
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["rmsn_bwd.cu", "rmsn_device.cuh"]
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -81,22 +80,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
 
 
-def _source_digest() -> str:
+def _source_digest(files) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "rmsnorm_fwd_bwd_persistent_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the backward (main + dW reduce) from the committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", "bwd_traffic.json")
+def recorded_traffic(op: str):
+    """DRAM bytes (read + write) per launch of `op` from the committed ncu summary, if it
+    was taken on the current sources of that op's kernels; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            d = json.load(f)
-        if d.get("source_digest") == _source_digest():
+            d = json.load(f)[op]
+        if d.get("source_digest") == _source_digest(d["sources"]):
             return int(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -410,7 +409,7 @@ def run_ours(args, world, rank, local):
                    "bytes": step.bytes[op], "launches": Step.LAUNCHES[op]}
     dom = max(Step.OPS, key=lambda o: op_ms[o])
     achieved = step.bytes[dom] / (op_ms[dom] * 1e-3) / 1e9
-    traffic = recorded_traffic() if dom == "bwd" else None
+    traffic = recorded_traffic(dom)
 
     if rank != 0:
         return 0

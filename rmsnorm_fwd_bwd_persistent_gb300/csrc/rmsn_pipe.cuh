@@ -51,23 +51,28 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One poll of the phase with parity `parity`.  While the phase is incomplete the thread
+// may be suspended for up to kSuspendNs (it resumes as soon as the phase completes), so a
+// waiting warp takes few issue slots.
+constexpr uint32_t kSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
         : "memory");
     return done != 0;
 }
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Gives up (returns
-// false) after `limit_ns` of %globaltimer time or after kMaxPolls polls, whichever comes
-// first, so the wait ends even if the timer does not advance.  Polls after the first few
-// back off with __nanosleep.
-constexpr uint32_t kMaxPolls = 1u << 22;
+// false) after `limit_ns` of %globaltimer time or after kMaxPolls polls (each suspends for
+// at most kSuspendNs), whichever comes first, so the wait ends even if the timer does not
+// advance.  Polls after the first few back off with __nanosleep.
+constexpr uint32_t kMaxPolls = 1u << 16;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_test(bar, parity)) return true;
