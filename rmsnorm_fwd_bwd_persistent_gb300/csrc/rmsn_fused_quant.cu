@@ -46,27 +46,67 @@ struct FusedArgs {
     float eps;
 };
 
-// Round-to-nearest-even, saturating conversion of two floats to E4M3 (a in the low byte).
-__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+// scale = RN(amax / 448) for a bf16 value amax in [2^-100, max finite]: Markstein's
+// correction of the product with c = RN(1/448) (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", 1990): q0 = RN(amax * c), the residual
+// r = amax - 448 * q0 is exact in one FMA, and RN(q0 + r * c) is the correctly rounded
+// quotient.  Checked exhaustively against the exact quotient for every bf16 value of that
+// range (29184 values; tests/test_oracle_pins.py re-derives the check).  Outside it (0,
+// tiny, inf) the IEEE division is used.
+__device__ __forceinline__ float scale_of(float amax) {
+    constexpr float c = 1.0f / 448.0f;  // RN(1/448)
+    if (!(amax >= 0x1p-100f && amax <= 0x1.fep127f)) return __fdiv_rn(amax, 448.0f);
+    const float q0 = __fmul_rn(amax, c);
+    const float r = __fmaf_rn(-q0, 448.0f, amax);
+    return __fmaf_rn(r, c, q0);
 }
-__device__ __forceinline__ uint32_t to_e4m3x2(f2 v) { return to_e4m3x2(f2_lo(v), f2_hi(v)); }
 
-// E4M3 codes of RN(n / s) for a pair of bf16-rounded normed values n, where s > 0 is the
-// block scale and y = RN(1 / s) (s and y normal).  The IEEE quotient Q = RN(n / s) is not
-// formed directly: q0 = RN(n * y) satisfies |q0 - Q| < 3.01 * 2^-24 * |q0| (y is within
-// 2^-24 relative of 1/s, and each rounding adds at most 2^-24 relative), so
+// y ~ 1/s for a normal s within 2^-23 relative: the approximate reciprocal followed by one
+// Newton-Raphson step y1 = y0 + y0 * (1 - s * y0) (the step squares the relative error of
+// y0 and adds at most one rounding).
+__device__ __forceinline__ float recip_of(float s) {
+    float y0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(s));
+    return __fmaf_rn(y0, __fmaf_rn(-s, y0, 1.0f), y0);
+}
+
+// E4M3 codes (round to nearest even, saturating) of two FP32 pairs, packed into one word:
+// a.lo in byte 0, a.hi in byte 1, b.lo in byte 2, b.hi in byte 3.
+__device__ __forceinline__ uint32_t e4m3x4(f2 a, f2 b) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(f2_lo(a)), "f"(f2_hi(a)), "f"(f2_lo(b)), "f"(f2_hi(b)));
+    return r;
+}
+
+// E4M3 codes of RN(n / s) for the eight bf16-rounded normed values of a 16-byte vector
+// (four pairs), s > 0 the block scale and y ~ 1/s within 2^-23 relative (s and y normal),
+// packed as two words (element order).  The IEEE quotient Q = RN(n / s) is not formed
+// directly: q0 = RN(n * y) satisfies |q0 - Q| < 4.01 * 2^-24 * |q0|, so
 // lo = RN(q0 * (1 - 2^-21)) and hi = RN(q0 * (1 + 2^-21)) bracket Q.  The conversion is
-// monotone, so if lo and hi give the same code, that is the code of Q.  Otherwise (when Q
-// lies within a few units in the last place of an E4M3 rounding boundary: about one
-// element in 10^5) the code is taken from the IEEE division itself.  Values below 2^-100
-// in magnitude have the signed-zero code on every path.
-__device__ __forceinline__ uint32_t quotient_codes(f2 n, f2 y, float s) {
-    const f2 q0 = mul2(n, y);
-    const uint32_t clo = to_e4m3x2(mul2(q0, f2_splat(1.0f - 0x1p-21f)));
-    const uint32_t chi = to_e4m3x2(mul2(q0, f2_splat(1.0f + 0x1p-21f)));
-    if (clo == chi) return clo;
-    return to_e4m3x2(__fdiv_rn(f2_lo(n), s), __fdiv_rn(f2_hi(n), s));
+// monotone, so where lo and hi give the same code it is the code of Q.  If any element of
+// the vector differs (Q within a few units in the last place of an E4M3 rounding boundary:
+// about one element in 10^5), the vector's codes are taken from the IEEE division itself.
+__device__ __forceinline__ uint2 quotient_codes(const f2 (&n)[4], float y, float s) {
+    const f2 y2 = f2_splat(y);
+    const f2 dn = f2_splat(1.0f - 0x1p-21f), up = f2_splat(1.0f + 0x1p-21f);
+    f2 q0[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q0[i] = mul2(n[i], y2);
+    const uint32_t lo0 = e4m3x4(mul2(q0[0], dn), mul2(q0[1], dn));
+    const uint32_t lo1 = e4m3x4(mul2(q0[2], dn), mul2(q0[3], dn));
+    const uint32_t hi0 = e4m3x4(mul2(q0[0], up), mul2(q0[1], up));
+    const uint32_t hi1 = e4m3x4(mul2(q0[2], up), mul2(q0[3], up));
+    if (((lo0 ^ hi0) | (lo1 ^ hi1)) == 0) return make_uint2(lo0, lo1);
+    f2 qd[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        qd[i] = f2_make(__fdiv_rn(f2_lo(n[i]), s), __fdiv_rn(f2_hi(n[i]), s));
+    return make_uint2(e4m3x4(qd[0], qd[1]), e4m3x4(qd[2], qd[3]));
 }
 
 template <int NCH>
@@ -112,7 +152,10 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
         const int64_t base = row * H;
         const bool ok = ring_wait_full(ring, at, a.limit_ns, a.err);
         const uint8_t* st = ring.stage(at.s);
+        // h = bf16(x + residual), written back to residual; sum of h^2 in two chains (even
+        // and odd elements) added at the end
         uint4 hv[NCH];
+        f2 ss2 = f2_splat(0.f);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
@@ -123,18 +166,12 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
 #pragma unroll
             for (int i = 0; i < NP; ++i) rp[i] = add2(xp[i], rp[i]);
             hv[c] = Pairs<__nv_bfloat16>::put(rp);  // h rounded once to bf16
+            if (in) st_stream(a.res + base + (int64_t)v * VEC, hv[c]);
+            Pairs<__nv_bfloat16>::get(hv[c], rp);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) ss2 = fma2(rp[i], rp[i], ss2);
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, at);
-        f2 ss2 = f2_splat(0.f);  // even and odd elements, added at the end
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int v = c * NC + t;
-            if (ok && v < nvec) st_stream(a.res + base + (int64_t)v * VEC, hv[c]);
-            f2 hp[NP];
-            Pairs<__nv_bfloat16>::get(hv[c], hp);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) ss2 = fma2(hp[i], hp[i], ss2);
-        }
         float ss = __fadd_rn(f2_lo(ss2), f2_hi(ss2));
         if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
         const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
@@ -165,25 +202,22 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float scale = __fdiv_rn(amax, 448.0f);
+            const float scale = scale_of(amax);
             if (in && (t & 15) == 0) a.scale[(int64_t)(v >> 4) * a.ld + row] = scale;
 
-            uint32_t codes[NP];
-            if (amax >= 0x1p-100f) {
-                const f2 y2 = f2_splat(__frcp_rn(scale));
-#pragma unroll
-                for (int i = 0; i < NP; ++i) codes[i] = quotient_codes(np_[i], y2, scale);
-            } else if (scale > 0.f) {
+            uint2 codes;
+            if (amax >= 0x1p-100f && amax <= 0x1.fep127f) {
+                codes = quotient_codes(np_, recip_of(scale), scale);
+            } else if (scale > 0.f) {  // tiny or infinite amax: the IEEE division
+                f2 qd[NP];
 #pragma unroll
                 for (int i = 0; i < NP; ++i)
-                    codes[i] = to_e4m3x2(__fdiv_rn(f2_lo(np_[i]), scale), __fdiv_rn(f2_hi(np_[i]), scale));
+                    qd[i] = f2_make(__fdiv_rn(f2_lo(np_[i]), scale), __fdiv_rn(f2_hi(np_[i]), scale));
+                codes = make_uint2(e4m3x4(qd[0], qd[1]), e4m3x4(qd[2], qd[3]));
             } else {  // amax == 0: the signed zero of each element
-#pragma unroll
-                for (int i = 0; i < NP; ++i) codes[i] = to_e4m3x2(np_[i]);
+                codes = make_uint2(e4m3x4(np_[0], np_[1]), e4m3x4(np_[2], np_[3]));
             }
-            if (in)
-                __stcs(reinterpret_cast<uint2*>(a.q + base + (int64_t)v * VEC),
-                       make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16)));
+            if (in) __stcs(reinterpret_cast<uint2*>(a.q + base + (int64_t)v * VEC), codes);
         }
     }
 }
