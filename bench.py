@@ -190,6 +190,18 @@ class Step:
             "bwd": wl.bwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype),
             "fused_quant": wl.fused_quant_bytes(f.T, f.H),
         }
+        # the residual training variant at the same shape (timed apart from the step)
+        r = wl.RESIDUAL_MAIN
+        self.rx, self.rres, self.rdy, self.rg, self.rw = wl.residual_inputs(r, dev, seed + 2)
+        self.ry, self.rh, self.rdx = (torch.empty_like(self.rx) for _ in range(3))
+        self.rrstd = torch.empty(r.T, device=dev)
+        self.rdw = torch.empty(r.H, device=dev)
+        self.bytes_extra = {
+            "fwd_residual": wl.fwd_residual_bytes(r.T, r.H, r.x_dtype, r.w_dtype),
+            "bwd_residual": wl.bwd_residual_bytes(r.T, r.H, r.x_dtype, r.w_dtype),
+        }
+        rmsn.rmsnorm_fwd_residual(self.rx, self.rres, self.rw, r.eps, y=self.ry, h_new=self.rh,
+                                  rstd=self.rrstd)
         # fwd writes rstd for the bwd once, so the bwd sees the forward's saved value
         rmsn.rmsnorm_fwd(self.x, self.w, self.eps, y=self.y, rstd=self.rstd)
 
@@ -211,11 +223,22 @@ class Step:
                                                     q=self.q, block_scale=self.scale,
                                                     normed=self.normed)
 
+    def fwd_residual(self):
+        self.rmsn.rmsnorm_fwd_residual(self.rx, self.rres, self.rw, self.eps, y=self.ry,
+                                       h_new=self.rh, rstd=self.rrstd)
+
+    def bwd_residual(self):
+        self.rmsn.rmsnorm_bwd_residual(self.rdy, self.rh, self.rw, self.rrstd, self.rg,
+                                       deterministic=True, compensated=False, workspace=self.ws,
+                                       dx_total=self.rdx, dw=self.rdw)
+
     OPS = ("fwd", "bwd", "fused_quant")
-    LAUNCHES = {"fwd": 1, "bwd": 2, "fused_quant": 1}
+    EXTRA_OPS = ("fwd_residual", "bwd_residual")
+    LAUNCHES = {"fwd": 1, "bwd": 2, "fused_quant": 1, "fwd_residual": 1, "bwd_residual": 2}
 
     def run_op(self, name):
-        {"fwd": self.fwd, "bwd": self.bwd, "fused_quant": self.fused}[name]()
+        {"fwd": self.fwd, "bwd": self.bwd, "fused_quant": self.fused,
+         "fwd_residual": self.fwd_residual, "bwd_residual": self.bwd_residual}[name]()
 
 
 def time_steps(step: Step, steps: int, warmup: int, world: int):
@@ -242,6 +265,33 @@ def time_steps(step: Step, steps: int, warmup: int, world: int):
     wall = time.perf_counter() - t0
     per_op = {op: [s.elapsed_time(e) for s, e in ev[op]] for op in Step.OPS}
     return per_op, wall
+
+
+def time_extra(step: Step, steps: int, warmup: int):
+    """The residual training variant (not part of the step), same protocol: L2 flushed
+    before each op, CUDA events around each call; mean us per op."""
+    for _ in range(warmup):
+        for op in Step.EXTRA_OPS:
+            step.flush()
+            step.run_op(op)
+    ev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)] for op in Step.EXTRA_OPS}
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for op in Step.EXTRA_OPS:
+            step.flush()
+            s, e = ev[op][i]
+            s.record()
+            step.run_op(op)
+            e.record()
+    torch.cuda.synchronize()
+    out = {}
+    for op in Step.EXTRA_OPS:
+        ms = statistics.mean(s.elapsed_time(e) for s, e in ev[op])
+        gbs = step.bytes_extra[op] / (ms * 1e-3) / 1e9
+        out[op] = {"us_mean": ms * 1e3, "gbs": gbs, "bytes": step.bytes_extra[op],
+                   "launches": Step.LAUNCHES[op]}
+    return out
 
 
 def time_e2e(step: Step, steps: int, warmup: int):
@@ -397,6 +447,7 @@ def run_ours(args, world, rank, local):
     max_ms, total_bytes = aggregate(step_ms, step_bytes, world)
     value = total_bytes / (max_ms * 1e-3) / 1e9
 
+    extra = time_extra(step, min(args.steps, 200), 3)
     e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
     e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
@@ -432,10 +483,11 @@ def run_ours(args, world, rank, local):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": step.bytes[dom],
                      "peak_source": peak_src},
+        "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
-        "gpu_launches": sum(Step.LAUNCHES.values()) * args.steps,
+        "gpu_launches": sum(Step.LAUNCHES[o] for o in Step.OPS) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }

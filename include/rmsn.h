@@ -187,6 +187,55 @@ int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void*
                                       rmsn_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * rmsnorm_fwd_residual -- the forward fused with the residual add of a transformer block.
+ *
+ * Source: FlashInfer PR #5741 "cake_rmsnorm_train", Design/Forward ("optionally fused with
+ * a residual add: h_new = bf16(x + residual) is normalized") and API (the forward with
+ * `residual=` returns y, rstd and h_new).
+ *
+ *   h_new[i, j] = round(x[i, j] + residual[i, j])      (one rounding to x's dtype)
+ *   rstd[i]     = 1 / sqrt(mean_j(h_new[i, j]^2) + eps) (FP32)
+ *   y[i, j]     = round((h_new[i, j] * rstd[i]) * w[j])
+ *
+ * Arguments: as rmsnorm_fwd, plus
+ *   residual  device [T, H], x's dtype, row-major contiguous (read only)
+ *   h_new     device [T, H], x's dtype (written); it is the input of rmsnorm_bwd_residual
+ * Outputs may alias inputs of the same shape exactly (h_new == residual or h_new == x, the
+ * usual in-place residual update): every row is read before it is written.  Partial
+ * overlaps are not supported.  Alignment: x, residual, w, y, h_new 16 bytes; rstd 4 bytes.
+ * T == 0 writes nothing.  Returns RMSN_OK or an error status (see conventions).
+ * ---------------------------------------------------------------------------------- */
+int rmsnorm_fwd_residual(const void* x, const void* residual, int x_dtype, const void* w,
+                         int w_dtype, void* y, void* h_new, float* rstd, int64_t T, int64_t H,
+                         float eps, rmsn_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * rmsnorm_bwd_residual -- the backward of rmsnorm_fwd_residual.
+ *
+ * Source: FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward ("the residual variant
+ * adds g_residual into the dx it returns (dx_total), so both inputs of the residual add
+ * receive the same gradient tensor") and API (the backward takes h_new, w, rstd and
+ * g_residual).
+ *
+ *   dx_total[i, j] = round(rstd[i] * (dy*w - xhat * c_i)[j] + g_residual[i, j])  (FP32, one
+ *                    rounding to h's dtype), xhat = h * rstd, c_i = mean_j(dy*w*xhat)
+ *   dw[j]          = sum_i dy[i, j] * xhat[i, j]   (exactly as rmsnorm_bwd)
+ *
+ * Arguments: as rmsnorm_bwd with x = h (the forward's h_new), plus
+ *   g_residual  device [T, H], h's dtype: the gradient reaching h_new through the residual
+ *               stream (read only)
+ *   dx_total    device [T, H], h's dtype (written); it may alias dy or g_residual exactly
+ * The workspace and its size rule are those of rmsnorm_bwd (rmsnorm_bwd_workspace_bytes
+ * covers both calls); the deterministic, compensated and error behaviour is the same.
+ * Shapes: as rmsnorm_bwd, and H <= 14400 for bf16 (each ring stage holds three rows);
+ * larger H returns RMSN_ERR_UNSUPPORTED_SHAPE.
+ * ---------------------------------------------------------------------------------- */
+int rmsnorm_bwd_residual(const void* dy, const void* h, int x_dtype, const void* w, int w_dtype,
+                         const float* rstd, const void* g_residual, void* dx_total, float* dw,
+                         int64_t T, int64_t H, int deterministic, int compensated,
+                         void* workspace, size_t workspace_bytes, rmsn_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Launch policy (introspection).  The geometry the library uses for a call, computed
  * on the host without a GPU; `sm_count` is the device's multiprocessor count.
  *
@@ -194,11 +243,18 @@ int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void*
  * host function of the shape: vector width and warp count; persistent CTAs; several
  * warps per token row).
  * ---------------------------------------------------------------------------------- */
-typedef enum { RMSN_OP_FWD = 0, RMSN_OP_BWD = 1, RMSN_OP_FUSED_QUANT = 2 } rmsn_op;
+typedef enum {
+    RMSN_OP_FWD = 0,
+    RMSN_OP_BWD = 1,
+    RMSN_OP_FUSED_QUANT = 2,
+    RMSN_OP_FWD_RESIDUAL = 3,
+    RMSN_OP_BWD_RESIDUAL = 4
+} rmsn_op;
 
 /* Every kernel runs a persistent grid: a CTA is `consumer_warps` warps that share one
- * row at a time plus one producer warp whose first lane streams the CTA's rows into a
- * `stages`-deep shared-memory ring with bulk copies (cp.async.bulk, mbarrier-tracked);
+ * row at a time; the CTA's rows are streamed into a `stages`-deep shared-memory ring with
+ * bulk copies (cp.async.bulk, mbarrier-tracked) by the first lane of one extra producer
+ * warp (forward, fused quant) or by the first consumer thread (backward);
  * the weight vector is copied to shared memory once per CTA.  CTA b of a grid of G takes
  * the rows b, b + G, b + 2G, ...; the backward's CTAs are its row chunks.  At launch the
  * grid is clamped to the CTAs that are resident at once (the kernel's occupancy), so

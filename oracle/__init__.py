@@ -134,6 +134,45 @@ def rmsnorm_bwd(dy: np.ndarray, x: np.ndarray, w: np.ndarray, rstd: np.ndarray,
     return dx, dw
 
 
+# ------------------------------------------------------------- residual variants
+def residual_add(x: np.ndarray, res: np.ndarray) -> np.ndarray:
+    """h = x + res, rounded once to the storage format (FlashInfer PR #5741
+    "cake_rmsnorm_train", Design/Forward: h_new = bf16(x + residual)).  The binary64 sum of
+    two bf16 or two binary32 values is exact, so rounding it once (RNE) to the format is the
+    correctly rounded sum.  Same storage format as the inputs (float64 stays float64)."""
+    x, res = _c(x), _c(res)
+    assert x.shape == res.shape and _fmt(x) == _fmt(res)
+    if x.dtype == np.uint16:
+        s = bf16_bits_to_f64(x) + bf16_bits_to_f64(res)
+        return bf16_round(s).reshape(x.shape)
+    s = x.astype(np.float64) + res.astype(np.float64)
+    return s.astype(x.dtype)  # float32: RNE to binary32; float64: exact already
+
+
+def rmsnorm_fwd_residual(x: np.ndarray, res: np.ndarray, w: np.ndarray, eps: float,
+                         nthreads: int | None = None):
+    """Forward fused with the residual add (PR #5741, Design/Forward and API: the forward
+    with `residual=` returns y, rstd and h_new; h_new is what is normalized).
+    Returns (y [T,H] f64, rstd [T] f64, h_new in the storage format)."""
+    h = residual_add(x, res)
+    y, rstd = rmsnorm_fwd(h, w, eps, nthreads)
+    return y, rstd, h
+
+
+def rmsnorm_bwd_residual(dy: np.ndarray, h: np.ndarray, w: np.ndarray, rstd: np.ndarray,
+                         g_res: np.ndarray, nthreads: int | None = None,
+                         want_dx: bool = True, want_dw: bool = True):
+    """Backward of the residual forward at h = h_new (PR #5741, Design/Backward: the
+    residual variant adds g_residual into the dx it returns, dx_total; dw is unchanged).
+    Returns (dx_total [T,H] f64 or None, dw [H] f64 or None)."""
+    dx, dw = rmsnorm_bwd(dy, h, w, rstd, nthreads, want_dx=want_dx, want_dw=want_dw)
+    if want_dx:
+        g = _c(g_res)
+        gv = bf16_bits_to_f64(g) if g.dtype == np.uint16 else g.astype(np.float64)
+        dx = dx + gv.reshape(dx.shape)
+    return dx, dw
+
+
 # ------------------------------------------------------------------ fused add + norm
 def fused_add_rmsnorm(x_bits: np.ndarray, res_bits: np.ndarray, w_bits: np.ndarray,
                       eps: float, nthreads: int | None = None):

@@ -18,14 +18,15 @@ import torch
 __all__ = [
     "RMSN_F32", "RMSN_BF16", "RMSN_MAX_H", "RmsnError", "library_path", "load_library",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
+    "rmsnorm_fwd_residual", "rmsnorm_bwd_residual",
     "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan", "rmsn_set_policy",
     "rmsn_device_status",
-    "OP_FWD", "OP_BWD", "OP_FUSED_QUANT",
+    "OP_FWD", "OP_BWD", "OP_FUSED_QUANT", "OP_FWD_RESIDUAL", "OP_BWD_RESIDUAL",
 ]
 
 RMSN_F32, RMSN_BF16 = 0, 1
 RMSN_MAX_H = 16384
-OP_FWD, OP_BWD, OP_FUSED_QUANT = 0, 1, 2
+OP_FWD, OP_BWD, OP_FUSED_QUANT, OP_FWD_RESIDUAL, OP_BWD_RESIDUAL = 0, 1, 2, 3, 4
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "librmsn_gb300.so")
@@ -80,6 +81,13 @@ def load_library():
         L.fused_add_rmsnorm_fp8_block_quant.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _vp,
                                                         _i64, _i64, ctypes.c_float, _vp]
         L.rmsn_plan.restype = ctypes.c_int
+        L.rmsnorm_fwd_residual.restype = ctypes.c_int
+        L.rmsnorm_fwd_residual.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp,
+                                           _vp, _i64, _i64, ctypes.c_float, _vp]
+        L.rmsnorm_bwd_residual.restype = ctypes.c_int
+        L.rmsnorm_bwd_residual.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp,
+                                           _vp, _vp, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                           _vp, ctypes.c_size_t, _vp]
         L.rmsn_plan.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(_Plan)]
         L.rmsn_set_policy.restype = ctypes.c_int
@@ -195,6 +203,70 @@ def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.
                                         int(bool(compensated)), ws_ptr, ws_bytes, _stream(x))
     _check(st, "rmsnorm_bwd")
     return dx, dw
+
+
+# --------------------------------------------------------------- residual variants
+def rmsnorm_fwd_residual(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor,
+                         eps: float = 1e-6, y: torch.Tensor | None = None,
+                         h_new: torch.Tensor | None = None, rstd: torch.Tensor | None = None):
+    """h_new = round(x + residual); y, rstd = the forward of h_new.  Returns (y, rstd, h_new).
+    h_new may be `residual` itself (in-place update)."""
+    for t, n in ((x, "x"), (residual, "residual"), (w, "w")):
+        _cuda(t, n)
+    if x.dim() != 2 or residual.shape != x.shape or residual.dtype != x.dtype:
+        raise ValueError("x and residual must be [T, H] of one dtype")
+    T, H = x.shape
+    if w.shape != (H,):
+        raise ValueError("w must be [H]")
+    y = torch.empty_like(x) if y is None else y
+    h_new = torch.empty_like(x) if h_new is None else h_new
+    rstd = torch.empty(T, device=x.device, dtype=torch.float32) if rstd is None else rstd
+    for t, n in ((y, "y"), (h_new, "h_new"), (rstd, "rstd")):
+        _cuda(t, n)
+    if y.shape != x.shape or y.dtype != x.dtype or h_new.shape != x.shape or \
+            h_new.dtype != x.dtype or rstd.shape != (T,) or rstd.dtype != torch.float32:
+        raise ValueError("y and h_new must match x; rstd must be float32 [T]")
+    with torch.cuda.device(x.device):
+        st = load_library().rmsnorm_fwd_residual(_p(x), _p(residual), _dt(x), _p(w), _dt(w), _p(y),
+                                                 _p(h_new), _p(rstd), T, H, float(eps), _stream(x))
+    _check(st, "rmsnorm_fwd_residual")
+    return y, rstd, h_new
+
+
+def rmsnorm_bwd_residual(dy: torch.Tensor, h: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
+                         g_residual: torch.Tensor, deterministic: bool = True,
+                         compensated: bool = False, workspace: torch.Tensor | None = None,
+                         dx_total: torch.Tensor | None = None, dw: torch.Tensor | None = None):
+    """Backward of rmsnorm_fwd_residual at h = h_new: dx_total = dx + g_residual (FP32, one
+    rounding), dw as rmsnorm_bwd.  Returns (dx_total, dw)."""
+    for t, n in ((dy, "dy"), (h, "h"), (w, "w"), (rstd, "rstd"), (g_residual, "g_residual")):
+        _cuda(t, n)
+    if h.dim() != 2 or dy.shape != h.shape or dy.dtype != h.dtype or \
+            g_residual.shape != h.shape or g_residual.dtype != h.dtype:
+        raise ValueError("dy, h and g_residual must be [T, H] of one dtype")
+    T, H = h.shape
+    if w.shape != (H,) or rstd.shape != (T,) or rstd.dtype != torch.float32:
+        raise ValueError("w must be [H]; rstd float32 [T]")
+    dx_total = torch.empty_like(h) if dx_total is None else dx_total
+    dw = torch.empty(H, device=h.device, dtype=torch.float32) if dw is None else dw
+    _cuda(dx_total, "dx_total")
+    _cuda(dw, "dw")
+    if dx_total.shape != h.shape or dx_total.dtype != h.dtype or dw.shape != (H,) or \
+            dw.dtype != torch.float32:
+        raise ValueError("dx_total must match h; dw must be float32 [H]")
+    ws_ptr, ws_bytes = None, 0
+    if deterministic:
+        if workspace is None:
+            n = rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
+            workspace = torch.empty(max(n, 16), device=h.device, dtype=torch.uint8)
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_bytes = _p(workspace), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(h.device):
+        st = load_library().rmsnorm_bwd_residual(
+            _p(dy), _p(h), _dt(h), _p(w), _dt(w), _p(rstd), _p(g_residual), _p(dx_total), _p(dw),
+            T, H, int(bool(deterministic)), int(bool(compensated)), ws_ptr, ws_bytes, _stream(h))
+    _check(st, "rmsnorm_bwd_residual")
+    return dx_total, dw
 
 
 # ------------------------------------------------------------- fused add+norm+quant

@@ -7,6 +7,7 @@
 // function of (op, T, H, dtypes, SM count, shared memory per SM), testable without a GPU
 // (Liger-Kernel PR #1336: fast-path eligibility helpers as pure functions).
 #include <atomic>
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -35,13 +36,17 @@ struct Policy {
     int max_nch;
 };
 
-// Per op: FWD, BWD, FUSED.
-constexpr Policy kDefaultPolicy[3] = {
+// Per op: FWD, BWD, FUSED, FWD_RESIDUAL, BWD_RESIDUAL.
+constexpr int kOps = 5;
+constexpr Policy kDefaultPolicy[kOps] = {
     {0, 4, 2, 4, 16},  // forward: small CTAs, 4 per SM, two stages each
     {0, 2, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
     {0, 3, 2, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM
+    {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
+    {0, 2, 4, 2, 8},   // residual backward: as the backward, three rows per stage
 };
-Policy g_policy[3] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2]};
+Policy g_policy[kOps] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2],
+                         kDefaultPolicy[3], kDefaultPolicy[4]};
 std::mutex g_mu;
 
 Policy policy(int op) {
@@ -117,8 +122,9 @@ int pick_nch(const int (&set)[N], int64_t need) {
 // The grid is clamped again at launch to what is resident at once (fit_grid).
 int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem_sm,
          int64_t smem_cta, Launch* L, int64_t* ws_bytes) {
-    if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
+    if (op < 0 || op >= kOps) return RMSN_ERR_INVALID_ARG;
     if (!valid_dtype(x_dt) || !valid_dtype(w_dt)) return RMSN_ERR_INVALID_ARG;
+    const bool is_bwd = op == RMSN_OP_BWD || op == RMSN_OP_BWD_RESIDUAL;
     if (op == RMSN_OP_FUSED_QUANT && (x_dt != RMSN_BF16 || w_dt != RMSN_BF16))
         return RMSN_ERR_INVALID_ARG;
     if (T < 0 || sms <= 0) return RMSN_ERR_INVALID_ARG;
@@ -134,14 +140,16 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     }
     const int64_t need = cdiv(nvec, 32 * nw);
     int nch = 0;
-    if (op == RMSN_OP_FWD) nch = pick_nch(rmsn::kFwdNch, need);
-    else if (op == RMSN_OP_BWD) nch = pick_nch(rmsn::kBwdNch, need);
+    if (op == RMSN_OP_FWD || op == RMSN_OP_FWD_RESIDUAL) nch = pick_nch(rmsn::kFwdNch, need);
+    else if (is_bwd) nch = pick_nch(rmsn::kBwdNch, need);
     else nch = pick_nch(rmsn::kFusedNch, need);
     if (nch == 0 || nch > P.max_nch) return RMSN_ERR_UNSUPPORTED_SHAPE;
 
     const int64_t row_bytes = H * esize(x_dt);
     const int64_t row_pad = cdiv(row_bytes, 128) * 128;
-    const int64_t stage_bytes = (op == RMSN_OP_FWD) ? row_pad : 2 * row_pad;
+    // rows per stage: x; x and residual; x and dy; x, dy and g_residual
+    const int rows = op == RMSN_OP_FWD ? 1 : op == RMSN_OP_BWD_RESIDUAL ? 3 : 2;
+    const int64_t stage_bytes = rows * row_pad;
     const int64_t w_bytes = H * 4;  // w is staged in shared memory as FP32
     const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
     int cps = P.ctas_per_sm;
@@ -151,7 +159,7 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
         return (share - data_off) / stage_bytes;
     };
     // the backward holds two rows' stages at once (it takes rows two at a time)
-    const int64_t min_stages = (op == RMSN_OP_BWD) ? 2 : 1;
+    const int64_t min_stages = is_bwd ? 2 : 1;
     while (cps > 1 && stages_for(cps) < 2) --cps;
     int64_t stages = stages_for(cps);
     if (stages < min_stages) return RMSN_ERR_UNSUPPORTED_SHAPE;
@@ -173,7 +181,7 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     L->smem = data_off + stages * stage_bytes;
     L->err = nullptr;
     L->limit_ns = kWaitLimitNs;
-    if (ws_bytes) *ws_bytes = (op == RMSN_OP_BWD) ? grid * H * 4 * 2 : 0;
+    if (ws_bytes) *ws_bytes = is_bwd ? grid * H * 4 * 2 : 0;
     return RMSN_OK;
 }
 
@@ -259,7 +267,7 @@ const char* rmsn_status_string(int status) {
         case RMSN_ERR_UNSUPPORTED_SHAPE:
             return "unsupported shape (H must be a positive multiple of the 16-byte vector, "
                    "at most 16384; the fused quant needs H % 128 == 0; the fp32 backward "
-                   "at most 8192)";
+                   "at most 8192; the bf16 residual backward at most 14400)";
         case RMSN_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
         case RMSN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than rmsnorm_bwd_workspace_bytes";
         case RMSN_ERR_CUDA: return "CUDA error (launch or runtime call failed)";
@@ -283,7 +291,8 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
     out->vec_elems = 16 / esize(x_dtype);
     out->consumer_warps = L.nw;
     out->chunks_per_lane = L.nch;
-    out->threads = (op == RMSN_OP_BWD) ? L.nw * 32 : L.nw * 32 + 32;  // bwd: no producer warp
+    const bool is_bwd = op == RMSN_OP_BWD || op == RMSN_OP_BWD_RESIDUAL;
+    out->threads = is_bwd ? L.nw * 32 : L.nw * 32 + 32;  // backward: no producer warp
     out->stages = L.stages;
     out->ctas_per_sm = L.ctas_per_sm;
     out->grid = L.grid;
@@ -293,7 +302,7 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
 }
 
 int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages) {
-    if (op < 0 || op > 2) return RMSN_ERR_INVALID_ARG;
+    if (op < 0 || op >= kOps) return RMSN_ERR_INVALID_ARG;
     if (consumer_warps < 0 || consumer_warps > 8 ||
         (consumer_warps & (consumer_warps - 1)) != 0)
         return RMSN_ERR_INVALID_ARG;
@@ -352,7 +361,9 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
     if (!p) return 0;
     // The chunk count never exceeds min(T, SMs * CTAs per SM) whatever the dtypes, and
     // grows with T, so this bounds every call with T' <= T.
-    int64_t chunks = (int64_t)p->sms * policy(RMSN_OP_BWD).ctas_per_sm;
+    // (rmsnorm_bwd and rmsnorm_bwd_residual alike: the larger of their CTAs per SM)
+    const int cps = std::max(policy(RMSN_OP_BWD).ctas_per_sm, policy(RMSN_OP_BWD_RESIDUAL).ctas_per_sm);
+    int64_t chunks = (int64_t)p->sms * cps;
     if (chunks > T) chunks = T;
     return (size_t)(chunks * H * 4 * 2);
 }
@@ -381,6 +392,51 @@ int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w
     return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                       deterministic, compensated,
                                       static_cast<float*>(workspace), s));
+}
+
+int rmsnorm_fwd_residual(const void* x, const void* residual, int x_dtype, const void* w,
+                         int w_dtype, void* y, void* h_new, float* rstd, int64_t T, int64_t H,
+                         float eps, rmsn_stream_t stream) {
+    if (!valid_dtype(x_dtype) || !valid_dtype(w_dtype)) return RMSN_ERR_INVALID_ARG;
+    if (T < 0 || !(eps >= 0.f) || eps == __builtin_huge_valf()) return RMSN_ERR_INVALID_ARG;
+    if (H <= 0 || H > RMSN_MAX_H || H % (16 / esize(x_dtype)) != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return RMSN_OK;
+    if (!x || !residual || !w || !y || !h_new || !rstd) return RMSN_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(w, 16) || !aligned(y, 16) ||
+        !aligned(h_new, 16) || !aligned(rstd, 4))
+        return RMSN_ERR_MISALIGNED;
+    Launch L{};
+    int st = plan_current(RMSN_OP_FWD_RESIDUAL, T, H, x_dtype, w_dtype, &L, nullptr);
+    if (st != RMSN_OK) return st;
+    return from_cuda(rmsn::launch_fwd(L, x, x_dtype, w, w_dtype, y, rstd, T, H, eps,
+                                      reinterpret_cast<cudaStream_t>(stream), residual, h_new));
+}
+
+int rmsnorm_bwd_residual(const void* dy, const void* h, int x_dtype, const void* w, int w_dtype,
+                         const float* rstd, const void* g_residual, void* dx_total, float* dw,
+                         int64_t T, int64_t H, int deterministic, int compensated,
+                         void* workspace, size_t workspace_bytes, rmsn_stream_t stream) {
+    if (!valid_dtype(x_dtype) || !valid_dtype(w_dtype) || T < 0) return RMSN_ERR_INVALID_ARG;
+    if (H <= 0 || H > RMSN_MAX_H || H % (16 / esize(x_dtype)) != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (!dw) return RMSN_ERR_INVALID_ARG;
+    if (!aligned(dw, 16)) return RMSN_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) return from_cuda(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s));
+    if (!dy || !h || !w || !rstd || !g_residual || !dx_total) return RMSN_ERR_INVALID_ARG;
+    if (!aligned(dy, 16) || !aligned(h, 16) || !aligned(w, 16) || !aligned(g_residual, 16) ||
+        !aligned(dx_total, 16) || !aligned(rstd, 4))
+        return RMSN_ERR_MISALIGNED;
+    if (deterministic && !workspace)
+        return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (deterministic && !aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
+    Launch L{};
+    int64_t need = 0;
+    int st = plan_current(RMSN_OP_BWD_RESIDUAL, T, H, x_dtype, w_dtype, &L, &need);
+    if (st != RMSN_OK) return st;
+    if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
+    return from_cuda(rmsn::launch_bwd(L, dy, h, x_dtype, w, w_dtype, rstd, dx_total, dw, T, H,
+                                      deterministic, compensated,
+                                      static_cast<float*>(workspace), s, g_residual));
 }
 
 int fused_add_rmsnorm_fp8_block_quant(const void* x, void* residual, const void* w, uint8_t* q,

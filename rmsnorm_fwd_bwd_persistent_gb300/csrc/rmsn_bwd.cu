@@ -23,6 +23,10 @@
 //   compensated = 1: every term is added with TwoSum, row by row;
 //   compensated = 0: the two terms of a row pair are summed with one FMA and the block
 //                    sum is added with TwoSum ("blocked FP32 sums", blocks of two rows).
+// Residual variant (RES; FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward and
+// API: the backward adds g_residual into the dx it returns, dx_total): the stage holds the
+// x (= h_new), dy and g_residual rows; pass 2 adds g_residual to the FP32 dx before the
+// one rounding to x's dtype.
 // At the end of the strip the CTA writes its (high, low) partial row to the workspace
 // (deterministic mode) or adds high+low to dw with FP32 atomics.
 //
@@ -47,6 +51,7 @@ struct BwdArgs {
     void* dx;
     float* dw;   // non-deterministic mode: zeroed dw, atomically accumulated
     float* ws;   // deterministic mode: [n_chunks, H] high parts, then [n_chunks, H] low parts
+    const void* gres;  // residual variant: g_residual rows (x's dtype)
     unsigned* err;
     int64_t T;
     uint64_t limit_ns;
@@ -60,7 +65,7 @@ struct BwdArgs {
     int atomic;
 };
 
-template <typename TX, typename TW, int NCH, bool COMP>
+template <typename TX, typename TW, int NCH, bool COMP, bool RES>
 __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -70,7 +75,9 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     const int64_t nch = gridDim.x;
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / nch + 1;  // rows b, b + n, ... below T
-    const uint32_t dy_off = a.stage_bytes / 2;  // stage = [x row | dy row], each padded
+    // stage = [x row | dy row (| g_residual row)], each padded to the same size
+    const uint32_t dy_off = RES ? a.stage_bytes / 3 : a.stage_bytes / 2;
+    const uint32_t g_off = 2 * dy_off;
     stage_weights_f32<VEC>(static_cast<const TW*>(a.w), a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
@@ -100,9 +107,12 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
             }
             const int64_t off = (b + issued * nch) * (int64_t)a.row_bytes;
             uint8_t* dst = ring.stage(in.s);
-            mbar_arrive_expect_tx(&ring.full[in.s], 2 * a.row_bytes);
+            mbar_arrive_expect_tx(&ring.full[in.s], (RES ? 3 : 2) * a.row_bytes);
             bulk_load(dst, X + off, a.row_bytes, &ring.full[in.s]);
             bulk_load(dst + dy_off, DY + off, a.row_bytes, &ring.full[in.s]);
+            if constexpr (RES)
+                bulk_load(dst + g_off, static_cast<const uint8_t*>(a.gres) + off, a.row_bytes,
+                          &ring.full[in.s]);
         }
     };
     issue_below(ring.stages);
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     // KEEP: pass 1 keeps the pair's x and dy vectors in registers for pass 2, so both
     // stages are released before the barrier and the whole ring can be in flight during
     // pass 2.  Otherwise (long rows) pass 2 reads them from the stages again.
-    constexpr bool KEEP = NCH <= 2;
+    constexpr bool KEEP = NCH <= 2 && !RES;
     uint4 xr[2][NCH], dr[2][NCH];
 
     // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row
@@ -200,12 +210,22 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
                 Pairs<TX>::get(KEEP ? dr[0][c] : lds128(s0 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
                 for (int i = 0; i < NP; ++i) o[i] = mul2(rsa, fma2(xp[i], nca, mul2(dp[i], wp[i])));
+                if constexpr (RES) {  // dx_total = dx + g_residual, rounded once
+                    Pairs<TX>::get(lds128(s0 + g_off + (size_t)v * 16), xp);
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) o[i] = add2(o[i], xp[i]);
+                }
                 st_stream(dx0 + (int64_t)v * VEC, Pairs<TX>::put(o));
                 if constexpr (TWO) {
                     Pairs<TX>::get(KEEP ? xr[1][c] : lds128(s1 + (size_t)v * 16), xp);
                     Pairs<TX>::get(KEEP ? dr[1][c] : lds128(s1 + dy_off + (size_t)v * 16), dp);
 #pragma unroll
                     for (int i = 0; i < NP; ++i) o[i] = mul2(rsb, fma2(xp[i], ncb, mul2(dp[i], wp[i])));
+                    if constexpr (RES) {
+                        Pairs<TX>::get(lds128(s1 + g_off + (size_t)v * 16), xp);
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) o[i] = add2(o[i], xp[i]);
+                    }
                     st_stream(dx1 + (int64_t)v * VEC, Pairs<TX>::put(o));
                 }
             }
@@ -369,7 +389,8 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce_kernel(const float* __r
 // Launches the main kernel; *grid receives the number of chunks it ran with.
 template <typename TX, typename TW, int NCH, bool COMP>
 static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s, int64_t* grid) {
-    auto k = rmsnorm_bwd_kernel<TX, TW, NCH, COMP>;
+    auto k = a.gres ? rmsnorm_bwd_kernel<TX, TW, NCH, COMP, true>
+                    : rmsnorm_bwd_kernel<TX, TW, NCH, COMP, false>;
     const int threads = L.nw * 32;  // consumer warps only
     cudaError_t e = fit_grid((const void*)k, L, threads, grid);
     if (e != cudaSuccess) return e;
@@ -398,9 +419,11 @@ static cudaError_t dispatch_comp(const Launch& L, const BwdArgs& a, int comp, cu
 
 cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt, const void* w,
                        int w_dt, const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
-                       int deterministic, int compensated, float* ws, cudaStream_t s) {
-    BwdArgs a{dy, x, w, rstd, dx, dw, ws, L.err, T, L.limit_ns, (int)H, L.nw, L.stages,
-              L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off, deterministic ? 0 : 1};
+                       int deterministic, int compensated, float* ws, cudaStream_t s,
+                       const void* g_residual) {
+    BwdArgs a{dy, x, w, rstd, dx, dw, ws, g_residual, L.err, T, L.limit_ns, (int)H, L.nw,
+              L.stages, L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off,
+              deterministic ? 0 : 1};
     if (!deterministic) {
         cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), s);
         if (e != cudaSuccess) return e;

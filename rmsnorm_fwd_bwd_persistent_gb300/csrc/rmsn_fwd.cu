@@ -10,6 +10,11 @@
 // write y straight from registers.  w is copied to shared memory (as FP32) once per CTA.
 // The arithmetic runs on FP32 pairs (two IEEE operations per instruction, each rounded as
 // its scalar form would be).  x is read from HBM exactly once.
+//
+// Residual variant (RES; FlashInfer PR #5741 "cake_rmsnorm_train", Design/Forward and API:
+// the forward optionally fused with a residual add): the stage holds the x row and the
+// residual row, h_new = x + residual is rounded once to x's dtype and written out, and the
+// row that is normalized is h_new.
 #include "rmsn_device.cuh"
 #include "rmsn_internal.h"
 #include "rmsn_pipe.cuh"
@@ -21,6 +26,8 @@ struct FwdArgs {
     const void* w;
     void* y;
     float* rstd;
+    const void* res;  // residual variant: the residual rows (x's dtype)
+    void* h;          // residual variant: h_new = x + residual, rounded to x's dtype
     unsigned* err;
     int64_t T;
     uint64_t limit_ns;
@@ -34,7 +41,7 @@ struct FwdArgs {
     float eps;
 };
 
-template <typename TX, typename TW, int NCH>
+template <typename TX, typename TW, int NCH, bool RES>
 __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -52,8 +59,16 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
             const uint8_t* X = static_cast<const uint8_t*>(a.x);
             const int64_t issued = ring_produce(
                 ring, nrows, a.limit_ns, a.err, [&](int64_t k, uint8_t* dst, uint64_t* full) {
-                    mbar_arrive_expect_tx(full, a.row_bytes);
-                    bulk_load(dst, X + (b + k * G) * (int64_t)a.row_bytes, a.row_bytes, full);
+                    const int64_t off = (b + k * G) * (int64_t)a.row_bytes;
+                    if constexpr (RES) {  // stage = [x row | residual row]
+                        mbar_arrive_expect_tx(full, 2 * a.row_bytes);
+                        bulk_load(dst, X + off, a.row_bytes, full);
+                        bulk_load(dst + a.stage_bytes / 2,
+                                  static_cast<const uint8_t*>(a.res) + off, a.row_bytes, full);
+                    } else {
+                        mbar_arrive_expect_tx(full, a.row_bytes);
+                        bulk_load(dst, X + off, a.row_bytes, full);
+                    }
                 });
             ring_drain(ring, issued, a.limit_ns, a.err);
         }
@@ -76,8 +91,26 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
             xv[c] = (ok && v < nvec) ? lds128(st + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+            if constexpr (RES) {  // h_new = x + residual, rounded once to x's dtype
+                const uint4 rv = (ok && v < nvec) ? lds128(st + a.stage_bytes / 2 + (size_t)v * 16)
+                                                  : make_uint4(0, 0, 0, 0);
+                f2 hp[Pairs<TX>::NP], rp[Pairs<TX>::NP];
+                Pairs<TX>::get(xv[c], hp);
+                Pairs<TX>::get(rv, rp);
+#pragma unroll
+                for (int i = 0; i < Pairs<TX>::NP; ++i) hp[i] = add2(hp[i], rp[i]);
+                xv[c] = Pairs<TX>::put(hp);
+            }
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, at);
+        if constexpr (RES) {
+            TX* hr = static_cast<TX*>(a.h) + row * a.H;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const int v = c * NC + t;
+                if (ok && v < nvec) st_stream(hr + (int64_t)v * VEC, xv[c]);
+            }
+        }
 
         // sum of squares in two chains (even and odd elements), one pair instruction per two
         // elements; the chains are added at the end (a fixed order, same on every run)
@@ -115,7 +148,7 @@ __global__ void __launch_bounds__(288, 3) rmsnorm_fwd_kernel(FwdArgs a) {
 
 template <typename TX, typename TW, int NCH>
 static cudaError_t run(const Launch& L, const FwdArgs& a, cudaStream_t s) {
-    auto k = rmsnorm_fwd_kernel<TX, TW, NCH>;
+    auto k = a.res ? rmsnorm_fwd_kernel<TX, TW, NCH, true> : rmsnorm_fwd_kernel<TX, TW, NCH, false>;
     const int threads = L.nw * 32 + 32;
     int64_t grid = 0;
     cudaError_t e = fit_grid((const void*)k, L, threads, &grid);
@@ -139,9 +172,10 @@ static cudaError_t dispatch(const Launch& L, const FwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd(const Launch& L, const void* x, int x_dt, const void* w, int w_dt,
-                       void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s) {
-    FwdArgs a{x, w, y, rstd, L.err, T, L.limit_ns, (int)H, L.nw, L.stages, L.row_bytes,
-              L.stage_bytes, L.w_bytes, L.data_off, eps};
+                       void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s,
+                       const void* residual, void* h_new) {
+    FwdArgs a{x, w, y, rstd, residual, h_new, L.err, T, L.limit_ns, (int)H, L.nw, L.stages,
+              L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off, eps};
     if (x_dt == 1 && w_dt == 1) return dispatch<__nv_bfloat16, __nv_bfloat16>(L, a, s);
     if (x_dt == 1 && w_dt == 0) return dispatch<__nv_bfloat16, float>(L, a, s);
     if (x_dt == 0 && w_dt == 0) return dispatch<float, float>(L, a, s);

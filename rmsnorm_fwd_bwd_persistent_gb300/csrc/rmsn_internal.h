@@ -31,12 +31,16 @@ constexpr int kBwdNch[] = {1, 2, 3, 4, 6, 8};
 constexpr int kFusedNch[] = {1, 2, 3, 4, 6, 8};
 
 // dtype codes match rmsn_dtype: 0 = fp32, 1 = bf16
+// residual / h_new (forward) and g_residual (backward) select the residual variants
+// (null: the plain ops); they have x's dtype.
 cudaError_t launch_fwd(const Launch& L, const void* x, int x_dt, const void* w, int w_dt,
-                       void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s);
+                       void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s,
+                       const void* residual = nullptr, void* h_new = nullptr);
 
 cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt, const void* w,
                        int w_dt, const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
-                       int deterministic, int compensated, float* ws, cudaStream_t s);
+                       int deterministic, int compensated, float* ws, cudaStream_t s,
+                       const void* g_residual = nullptr);
 
 cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const void* w,
                          uint8_t* q, float* block_scale, int64_t scale_ld, void* normed,

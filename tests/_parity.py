@@ -111,6 +111,82 @@ def check_bwd(dy, x, w, rstd, deterministic=True, compensated=False, full_dw=Tru
     return out
 
 
+def check_fwd_residual(x, res, w, eps, inplace: bool = False) -> dict:
+    """rmsnorm_fwd_residual against the oracle: h_new bit-exact (one rounding of an exact
+    sum), y and rstd as the forward.  inplace: h_new is written over `res`."""
+    T, H = x.shape
+    res_in = res.clone()
+    ybuf, y = guarded((T, H), x.dtype, x.device)
+    rbuf, rstd = guarded((T,), torch.float32, x.device)
+    if inplace:
+        hbuf, h = None, res
+    else:
+        hbuf, h = guarded((T, H), x.dtype, x.device)
+    rmsn.rmsnorm_fwd_residual(x, res, w, eps, y=y, h_new=h, rstd=rstd)
+    torch.cuda.synchronize()
+    rows = _rows(T, H)
+    ridx = torch.from_numpy(rows).to(x.device)
+    y_ref, r_ref, h_ref = oracle.rmsnorm_fwd_residual(wl.to_oracle(x[ridx]), wl.to_oracle(res_in[ridx]),
+                                                      wl.to_oracle(w), eps)
+    h_dev = wl.to_oracle(h[ridx])
+    out = {"h_new": {"n_fail": int(np.count_nonzero(h_dev.view(np.uint16 if h_dev.dtype == np.uint16 else np.uint32)
+                                                    != h_ref.view(np.uint16 if h_ref.dtype == np.uint16 else np.uint32)))},
+           "rstd": gates.check_f32_rel(rstd.cpu().numpy()[rows], r_ref)}
+    y_dev = wl.to_oracle(y[ridx])
+    out["y"] = gates.check_bf16(y_dev, y_ref) if x.dtype == torch.bfloat16 else gates.check_f32_rel(y_dev, y_ref)
+    bufs = [ybuf, rbuf] + ([hbuf] if hbuf is not None else [])
+    out["guards"] = {"n_fail": int(not all(guards_ok(b) for b in bufs))}
+    out["device_status"] = {"n_fail": rmsn.rmsn_device_status()}
+    out["_h"], out["_rstd_dev"] = h, rstd
+    return out
+
+
+def check_bwd_residual(dy, h, w, rstd, g_res, deterministic=True, compensated=False,
+                       alias: str | None = None) -> dict:
+    """rmsnorm_bwd_residual against the oracle: dx_total = dx + g_residual (bf16 within one
+    ulp, widened by the a-priori FP32 bound of dx plus the rounding of the FP32 sum), dw as
+    rmsnorm_bwd.  alias: 'g' writes dx_total over g_residual, 'dy' over dy."""
+    T, H = h.shape
+    dy_in, g_in = dy.clone(), g_res.clone()
+    dwbuf, dw = guarded((H,), torch.float32, h.device)
+    if alias == "g":
+        dxbuf, dxt = None, g_res
+    elif alias == "dy":
+        dxbuf, dxt = None, dy
+    else:
+        dxbuf, dxt = guarded((T, H), h.dtype, h.device)
+    ws = None
+    if deterministic:
+        n = rmsn.rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
+        ws = torch.full((max(n, 16) // 4,), float("nan"), device=h.device, dtype=torch.float32)
+    rmsn.rmsnorm_bwd_residual(dy, h, w, rstd, g_res, deterministic=deterministic,
+                              compensated=compensated, workspace=ws, dx_total=dxt, dw=dw)
+    torch.cuda.synchronize()
+    rows = _rows(T, H)
+    ridx = torch.from_numpy(rows).to(h.device)
+    W = wl.to_oracle(w)
+    r_all = rstd.cpu().numpy().astype(np.float64)
+    DYs, Hs, Gs = wl.to_oracle(dy_in[ridx]), wl.to_oracle(h[ridx]), wl.to_oracle(g_in[ridx])
+    dxt_ref, _ = oracle.rmsnorm_bwd_residual(DYs, Hs, W, r_all[rows], Gs, want_dw=False)
+    dx_dev = wl.to_oracle(dxt[ridx])
+    out = {}
+    if h.dtype == torch.bfloat16:
+        dx_plain, _ = oracle.rmsnorm_bwd(DYs, Hs, W, r_all[rows], want_dw=False)
+        extra = gates.dx_fp32_bound(_f64(DYs), _f64(Hs), _f64(W), r_all[rows], dx_plain) + \
+            2.0 ** -23 * np.abs(dxt_ref)
+        out["dx_total"] = gates.check_bf16(dx_dev, dxt_ref, extra=extra)
+    else:
+        out["dx_total"] = gates.check_f32_rel(dx_dev, dxt_ref, row_rms_term=True)
+    _, dw_ref = oracle.rmsnorm_bwd_residual(wl.to_oracle(dy_in), wl.to_oracle(h), W, r_all,
+                                            wl.to_oracle(g_in), want_dx=False)
+    out["dw"] = gates.check_dw(dw.cpu().numpy(), dw_ref)
+    bufs = [dwbuf] + ([dxbuf] if dxbuf is not None else [])
+    out["guards"] = {"n_fail": int(not all(guards_ok(b) for b in bufs))}
+    out["device_status"] = {"n_fail": rmsn.rmsn_device_status()}
+    out["_dw_dev"] = dw
+    return out
+
+
 def check_fused(x, res, w, eps, ld_pad: int = 0) -> dict:
     T, H = x.shape
     ld = wl.round_up(T, 4) + ld_pad

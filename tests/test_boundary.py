@@ -87,10 +87,30 @@ def test_fused_argument_checks(lib):
     assert f(None, None, None, None, None, 0, None, 0, 256, 1e-6, None) == OK
 
 
+def test_residual_argument_checks(lib):
+    f = lib.rmsnorm_fwd_residual
+    assert f(A, A, 1, A, 1, A, A, A, 4, 7, 1e-6, None) == SHAPE        # H not a multiple of 8
+    assert f(A, A, 3, A, 1, A, A, A, 4, 64, 1e-6, None) == INVALID     # dtype code
+    assert f(A, None, 1, A, 1, A, A, A, 4, 64, 1e-6, None) == INVALID  # no residual
+    assert f(A, A, 1, A, 1, A, None, A, 4, 64, 1e-6, None) == INVALID  # no h_new
+    assert f(A, A + 8, 1, A, 1, A, A, A, 4, 64, 1e-6, None) == MISALIGNED
+    assert f(A, A, 1, A, 1, A, A + 4, A, 4, 64, 1e-6, None) == MISALIGNED
+    assert f(A, A, 1, A, 1, A, A, A, 4, 64, -1.0, None) == INVALID
+    assert f(None, None, 1, None, 1, None, None, None, 0, 64, 1e-6, None) == OK
+    b = lib.rmsnorm_bwd_residual
+    assert b(A, A, 1, A, 0, A, A, A, A, 4, 12, 1, 0, A, 1 << 20, None) == SHAPE
+    assert b(A, A, 1, A, 0, A, None, A, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID  # no g
+    assert b(A, A, 1, A, 0, A, A, None, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID  # no dx
+    assert b(A, A, 1, A, 0, A, A + 8, A, A, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
+    assert b(A, A, 1, A, 0, A, A, A, A + 4, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
+    assert b(A, A, 1, A, 0, A, A, A, A, 4, 64, 1, 0, None, 0, None) == WS_SMALL
+
+
 SM = 152
 
 
-@pytest.mark.parametrize("op", [rmsn.OP_FWD, rmsn.OP_BWD, rmsn.OP_FUSED_QUANT])
+@pytest.mark.parametrize("op", [rmsn.OP_FWD, rmsn.OP_BWD, rmsn.OP_FUSED_QUANT,
+                                rmsn.OP_FWD_RESIDUAL, rmsn.OP_BWD_RESIDUAL])
 @pytest.mark.parametrize("H", [8, 128, 256, 1536, 2048, 4096, 4104, 5120, 6144, 8192, 16384])
 @pytest.mark.parametrize("xd,wd", [(1, 1), (1, 0), (0, 0), (0, 1)])
 def test_plan_covers_rows(lib, op, H, xd, wd):
@@ -103,7 +123,8 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         with pytest.raises(rmsn.RmsnError):
             rmsn.rmsn_plan(op, 100, H, xd, wd)
         return
-    if op == rmsn.OP_BWD and xd == 0 and H > 8192:
+    is_bwd = op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL)
+    if (is_bwd and xd == 0 and H > 8192) or (op == rmsn.OP_BWD_RESIDUAL and H > 14400):
         with pytest.raises(rmsn.RmsnError):
             rmsn.rmsn_plan(op, 100, H, xd, wd)
         return
@@ -112,15 +133,16 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         lanes = 32 * p["consumer_warps"]
         assert p["vec_elems"] == vec
         assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
-        producer = 0 if op == rmsn.OP_BWD else 32                   # bwd: thread 0 feeds the ring
+        producer = 0 if is_bwd else 32                              # bwd: thread 0 feeds the ring
         assert p["threads"] == lanes + producer and p["threads"] <= 288
         assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
         row = H * (2 if xd == 1 else 4)
-        stage = -(-row // 128) * 128 * (1 if op == rmsn.OP_FWD else 2)
+        rows = {rmsn.OP_FWD: 1, rmsn.OP_BWD_RESIDUAL: 3}.get(op, 2)  # rows per stage
+        stage = -(-row // 128) * 128 * rows
         wpad = -(-(H * 4) // 128) * 128                           # w staged as FP32 in smem
         assert p["stages"] >= 1 and p["smem_bytes"] == 2048 + wpad + p["stages"] * stage
         assert p["ctas_per_sm"] * (p["smem_bytes"] + 1024) <= 233472  # fits the SM
-        if p["ctas_per_sm"] > 1 or op == rmsn.OP_BWD:
+        if p["ctas_per_sm"] > 1 or is_bwd:
             assert p["stages"] >= 2                                 # bwd holds two rows
         if op == rmsn.OP_FUSED_QUANT:
             assert lanes % 16 == 0                                  # 16 lanes hold one block

@@ -441,3 +441,94 @@ def test_fused_byte_model_against_page_example():
     new = workloads.fused_quant_bytes(M, H)
     old = new - 2 * H + 2 * M * H
     assert abs(f["gbps_weight_as_H"] * old / new - f["gbps_weight_as_MxH"]) < 0.001 * 4397
+
+
+# ================================================================ residual variants
+# FlashInfer PR #5741 "cake_rmsnorm_train", Design (forward with residual: h_new =
+# bf16(x + residual) is normalized; backward: dx_total = dx + g_residual) and API.
+def _res_loss(x, r, w, dy, g, eps):
+    """L = sum(dy * y(x + r)) + sum(g * (x + r)): the loss whose gradient with respect to x
+    (and to r) is dx_total (FP64, h unrounded)."""
+    y, _, h = oracle.rmsnorm_fwd_residual(x, r, w, eps)
+    return float(np.sum(dy * y) + np.sum(g * h))
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.3])
+def test_residual_dx_total_finite_differences(eps):
+    T, H, step = 3, 8, 1e-6
+    x = _rng(40).standard_normal((T, H))
+    r = _rng(41).standard_normal((T, H))
+    dy = _rng(42).standard_normal((T, H))
+    g = _rng(43).standard_normal((T, H))
+    w = 1 + 0.1 * _rng(44).standard_normal(H)
+    _, rstd, h = oracle.rmsnorm_fwd_residual(x, r, w, eps)
+    dxt, _ = oracle.rmsnorm_bwd_residual(dy, h, w, rstd, g)
+    fdx, fdr = np.zeros_like(x), np.zeros_like(x)
+    for i in range(T):
+        for j in range(H):
+            for arr, fd in ((x, fdx), (r, fdr)):
+                ap, am = arr.copy(), arr.copy()
+                ap[i, j] += step
+                am[i, j] -= step
+                args_p = (ap, r) if arr is x else (x, ap)
+                args_m = (am, r) if arr is x else (x, am)
+                fd[i, j] = (_res_loss(*args_p, w, dy, g, eps) -
+                            _res_loss(*args_m, w, dy, g, eps)) / (2 * step)
+    np.testing.assert_allclose(dxt, fdx, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dxt, fdr, rtol=1e-6, atol=1e-8)  # both inputs, one gradient
+
+
+def test_residual_dw_finite_differences():
+    T, H, step, eps = 4, 8, 1e-6, 1e-6
+    x, r = _rng(45).standard_normal((T, H)), _rng(46).standard_normal((T, H))
+    dy, g = _rng(47).standard_normal((T, H)), _rng(48).standard_normal((T, H))
+    w = 1 + 0.1 * _rng(49).standard_normal(H)
+    _, rstd, h = oracle.rmsnorm_fwd_residual(x, r, w, eps)
+    _, dw = oracle.rmsnorm_bwd_residual(dy, h, w, rstd, g)
+    for j in range(H):
+        wp, wm = w.copy(), w.copy()
+        wp[j] += step
+        wm[j] -= step
+        fd = (_res_loss(x, r, wp, dy, g, eps) - _res_loss(x, r, wm, dy, g, eps)) / (2 * step)
+        assert dw[j] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+def test_residual_zero_reduces_to_plain_ops():
+    x = _bf16_bits(torch.randn(5, 64, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16))
+    w = _bf16_bits((1 + 0.1 * torch.randn(64, generator=torch.Generator().manual_seed(4))).to(torch.bfloat16))
+    zero = np.zeros_like(x)
+    y_r, rstd_r, h = oracle.rmsnorm_fwd_residual(x, zero, w, 1e-6)
+    y, rstd = oracle.rmsnorm_fwd(x, w, 1e-6)
+    assert np.array_equal(h, x)
+    assert np.array_equal(y_r, y) and np.array_equal(rstd_r, rstd)
+    dy = _bf16_bits(torch.randn(5, 64, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16))
+    dxt, dw_r = oracle.rmsnorm_bwd_residual(dy, h, w, rstd, zero)
+    dx, dw = oracle.rmsnorm_bwd(dy, x, w, rstd)
+    assert np.array_equal(dxt, dx) and np.array_equal(dw_r, dw)
+
+
+def test_residual_add_exact_and_rounded():
+    # small integers: every sum is exact in bf16 and in binary32
+    a = np.arange(-64, 64, dtype=np.float32).reshape(8, 16)
+    b = a[::-1].copy()
+    assert np.array_equal(oracle.residual_add(a, b), a + b)
+    ab, bb = _bf16_bits(torch.from_numpy(a).to(torch.bfloat16)), _bf16_bits(torch.from_numpy(b).to(torch.bfloat16))
+    assert np.array_equal(oracle.bf16_bits_to_f64(oracle.residual_add(ab, bb)), (a + b).astype(np.float64))
+    # 1 + 2^-8 lies halfway between the bf16 neighbours 1 and 1 + 2^-7: ties to even gives 1;
+    # 1 + 3*2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6 and ties to 1 + 2^-6
+    one = _bf16_bits(torch.tensor([[1.0, 1.0]], dtype=torch.bfloat16))
+    d = _bf16_bits(torch.tensor([[2.0 ** -8, 3 * 2.0 ** -8]], dtype=torch.bfloat16))
+    got = oracle.bf16_bits_to_f64(oracle.residual_add(one, d))
+    assert got.tolist() == [[1.0, 1.0 + 2.0 ** -6]]
+
+
+def test_residual_g_only_shifts_dx():
+    T, H = 3, 16
+    x = _rng(50).standard_normal((T, H)).astype(np.float32)
+    dy = _rng(51).standard_normal((T, H)).astype(np.float32)
+    w = (1 + 0.1 * _rng(52).standard_normal(H)).astype(np.float32)
+    _, rstd = oracle.rmsnorm_fwd(x, w, 1e-6)
+    g = np.full((T, H), 0.25, np.float32)  # a constant gradient through the residual stream
+    dxt, _ = oracle.rmsnorm_bwd_residual(dy, x, w, rstd, g)
+    dx, _ = oracle.rmsnorm_bwd(dy, x, w, rstd)
+    np.testing.assert_allclose(dxt - dx, 0.25, rtol=0, atol=1e-15)

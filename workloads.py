@@ -39,6 +39,9 @@ MAIN_BF16 = Workload("rmsnorm_t8192_h4096_bf16", 8192, 4096, torch.bfloat16, tor
 FUSED_QUANT = Workload("fused_add_rmsnorm_fp8_t2048_h4096_bf16", 2048, 4096, torch.bfloat16,
                        torch.bfloat16, res_std=2.0)
 # the same fused op at the headline shape (the step the benchmark times)
+RESIDUAL_MAIN = Workload("rmsnorm_residual_t8192_h4096_bf16", 8192, 4096, torch.bfloat16,
+                         torch.bfloat16, res_std=2.0)
+
 FUSED_QUANT_MAIN = Workload("fused_add_rmsnorm_fp8_t8192_h4096_bf16", 8192, 4096,
                             torch.bfloat16, torch.bfloat16, res_std=2.0)
 # deterministic backward sweep: bf16 x/dy, fp32 w
@@ -89,6 +92,20 @@ def fused_inputs(wl: Workload, device="cpu", seed: int = 0, T: int | None = None
     return x, res, w
 
 
+def residual_inputs(wl: Workload, device="cpu", seed: int = 0, T: int | None = None):
+    """Inputs of the residual training variant: x, residual, dy, g_residual [T, H] (x_dtype)
+    and w [H] (w_dtype), drawn in the order x, residual, dy, g_residual, w; residual has
+    standard deviation res_std, the others as in fwd_bwd_inputs."""
+    T = wl.T if T is None else T
+    g = _gen(device, seed)
+    x = _normal((T, wl.H), wl.x_std, wl.x_dtype, g, device)
+    res = _normal((T, wl.H), wl.res_std, wl.x_dtype, g, device)
+    dy = _normal((T, wl.H), wl.dy_std, wl.x_dtype, g, device)
+    g_res = _normal((T, wl.H), wl.dy_std, wl.x_dtype, g, device)
+    w = weight(wl.H, wl.w_dtype, g, device)
+    return x, res, dy, g_res, w
+
+
 def round_up(a: int, b: int) -> int:
     return (a + b - 1) // b * b
 
@@ -122,6 +139,18 @@ def bwd_bytes(T: int, H: int, x_dtype: torch.dtype, w_dtype: torch.dtype) -> int
     write dw (FlashInfer PR #5741, Performance: bwd 3 x 2TH + 4T + 4H for bf16)."""
     s, sw = _esize(x_dtype), _esize(w_dtype)
     return 3 * T * H * s + H * sw + 4 * T + 4 * H
+
+
+def fwd_residual_bytes(T: int, H: int, x_dtype: torch.dtype, w_dtype: torch.dtype) -> int:
+    """The forward's bytes plus reading residual and writing h_new (FlashInfer PR #5741,
+    Performance: fwd ... [+ 2TH residual in, 2TH h_new out] for bf16)."""
+    return fwd_bytes(T, H, x_dtype, w_dtype) + 2 * T * H * _esize(x_dtype)
+
+
+def bwd_residual_bytes(T: int, H: int, x_dtype: torch.dtype, w_dtype: torch.dtype) -> int:
+    """The backward's bytes plus reading g_residual (FlashInfer PR #5741, Performance:
+    bwd ... [+ 2TH] for bf16)."""
+    return bwd_bytes(T, H, x_dtype, w_dtype) + T * H * _esize(x_dtype)
 
 
 def fused_quant_bytes(T: int, H: int) -> int:
