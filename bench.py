@@ -294,6 +294,46 @@ def time_extra(step: Step, steps: int, warmup: int):
     return out
 
 
+def time_small_t(dev, steps: int, warmup: int):
+    """The determinism sweep's T=65 rows (bf16 x/dy, fp32 w) through the deterministic
+    backward, on the one-launch small-T route and on the strip route; mean us per call,
+    L2 flushed before each call."""
+    import dataclasses
+    import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    rd = flush.view(torch.float32)[: (FLUSH_BYTES // 2) // 4]
+    old = rmsn.rmsn_small_t_max()
+    out = {}
+    try:
+        for H in wl.DET_SWEEP_H:
+            c = dataclasses.replace(wl.DET_SWEEP[0], T=65, H=H)
+            x, dy, w = wl.fwd_bwd_inputs(c, dev, 0)
+            _, rstd = rmsn.rmsnorm_fwd(x, w, c.eps)
+            dx, dw = torch.empty_like(x), torch.empty(H, device=dev)
+            ws = torch.empty(max(rmsn.rmsnorm_bwd_workspace_bytes(65, H, False, dev), 16),
+                             device=dev, dtype=torch.uint8)
+            row = {}
+            for route, t_max in (("small_t", old if old > 0 else 256), ("strip", 0)):
+                rmsn.rmsn_set_small_t_max(t_max)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(steps)]
+                for i in range(warmup + steps):
+                    flush.zero_()
+                    rd.sum()
+                    if i >= warmup:
+                        ev[i - warmup][0].record()
+                    rmsn.rmsnorm_bwd(dy, x, w, rstd, True, False, ws, dx, dw)
+                    if i >= warmup:
+                        ev[i - warmup][1].record()
+                torch.cuda.synchronize()
+                row[route] = statistics.mean(s.elapsed_time(e) for s, e in ev) * 1e3
+            out[f"T65_H{H}"] = {"us_small_t": row["small_t"], "us_strip": row["strip"],
+                                "bytes": wl.bwd_bytes(65, H, c.x_dtype, c.w_dtype)}
+    finally:
+        rmsn.rmsn_set_small_t_max(old)
+    return out
+
+
 def time_e2e(step: Step, steps: int, warmup: int):
     """The same step through the public API from pinned host buffers: every step copies
     its inputs host->device, runs the three ops and copies every output device->host."""
@@ -448,6 +488,7 @@ def run_ours(args, world, rank, local):
     value = total_bytes / (max_ms * 1e-3) / 1e9
 
     extra = time_extra(step, min(args.steps, 200), 3)
+    small = time_small_t(dev, min(args.steps, 200), 3)
     e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
     e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
@@ -484,6 +525,7 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic, "algorithmic_bytes": step.bytes[dom],
                      "peak_source": peak_src},
         "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
+        "bwd_small_t_route": small,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},

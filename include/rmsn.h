@@ -287,6 +287,21 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
  * values out of range (then nothing changes). */
 int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages);
 
+/* Small-T route of the deterministic backward (rmsnorm_bwd, rmsnorm_bwd_residual,
+ * rmsnorm_bwd_noalloc).  Source: miles-ext-kernels PR #15, Changes (#8813: a column-task
+ * weight-gradient kernel for the smallest T, one task per column slab summing the rows in
+ * a fixed order with FP32 compensation).  Calls with deterministic = 1 and T <= t_max run
+ * one kernel instead of the strip kernel and the column reduce: one CTA per row writes dx,
+ * one CTA per 64 columns sums dy*xhat over all rows in a fixed order (8 interleaved row
+ * sequences merged in order, compensated as `compensated` selects), and the workspace is
+ * not touched (it is still required, so a call's arguments do not depend on the route).
+ * dw bits depend on the route, so on (T, t_max) as well as on the other inputs.
+ * rmsn_set_small_t_max sets t_max for the process (0 disables the route; default 256;
+ * RMSN_ERR_INVALID_ARG above 2^20); changing it while calls are in flight on other host
+ * threads is a race.  rmsn_small_t_max returns the current value. */
+int rmsn_set_small_t_max(int64_t t_max);
+int64_t rmsn_small_t_max(void);
+
 /* ------------------------------------------------------------------------------------
  * rmsn_device_status -- every wait inside the kernels (a consumer waiting for a row to
  * land in shared memory, the producer waiting for a stage to be released) gives up after

@@ -20,7 +20,7 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "rmsnorm_fwd_residual", "rmsnorm_bwd_residual",
     "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan", "rmsn_set_policy",
-    "rmsn_device_status",
+    "rmsn_device_status", "rmsn_set_small_t_max", "rmsn_small_t_max",
     "OP_FWD", "OP_BWD", "OP_FUSED_QUANT", "OP_FWD_RESIDUAL", "OP_BWD_RESIDUAL",
 ]
 
@@ -81,6 +81,10 @@ def load_library():
         L.fused_add_rmsnorm_fp8_block_quant.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _vp,
                                                         _i64, _i64, ctypes.c_float, _vp]
         L.rmsn_plan.restype = ctypes.c_int
+        L.rmsn_set_small_t_max.restype = ctypes.c_int
+        L.rmsn_set_small_t_max.argtypes = [_i64]
+        L.rmsn_small_t_max.restype = _i64
+        L.rmsn_small_t_max.argtypes = []
         L.rmsnorm_fwd_residual.restype = ctypes.c_int
         L.rmsnorm_fwd_residual.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp,
                                            _vp, _i64, _i64, ctypes.c_float, _vp]
@@ -323,6 +327,16 @@ def rmsn_plan(op: int, T: int, H: int, x_dtype: int, w_dtype: int, compensated: 
 def rmsn_set_policy(op: int, consumer_warps: int = 0, ctas_per_sm: int = 0, max_stages: int = 0):
     _check(load_library().rmsn_set_policy(int(op), int(consumer_warps), int(ctas_per_sm),
                                           int(max_stages)), "rmsn_set_policy")
+
+
+def rmsn_set_small_t_max(t_max: int):
+    """Deterministic backward calls with T <= t_max run the one-launch column-task kernel
+    (0 disables).  Process-wide tuning hook."""
+    _check(load_library().rmsn_set_small_t_max(int(t_max)), "rmsn_set_small_t_max")
+
+
+def rmsn_small_t_max() -> int:
+    return int(load_library().rmsn_small_t_max())
 
 
 def rmsn_device_status(device: int | torch.device | None = None) -> int:

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librmsn_gb300.so")
 
-SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_fused_quant.cu"]
+SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_bwd_small.cu",
+           "rmsn_fused_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

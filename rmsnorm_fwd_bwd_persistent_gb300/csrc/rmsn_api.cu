@@ -49,6 +49,13 @@ Policy g_policy[kOps] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2]
                          kDefaultPolicy[3], kDefaultPolicy[4]};
 std::mutex g_mu;
 
+// Deterministic backward calls with T <= this take the one-launch column-task kernel
+// (rmsn_set_small_t_max).
+std::atomic<int64_t> g_small_t_max{256};  // measured break-even: T ~ 384-512 on GB300
+bool small_t(int deterministic, int64_t T) {
+    return deterministic && T <= g_small_t_max.load(std::memory_order_relaxed);
+}
+
 Policy policy(int op) {
     std::lock_guard<std::mutex> lk(g_mu);
     return g_policy[op];
@@ -317,6 +324,14 @@ int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages)
     return RMSN_OK;
 }
 
+int rmsn_set_small_t_max(int64_t t_max) {
+    if (t_max < 0 || t_max > (1 << 20)) return RMSN_ERR_INVALID_ARG;
+    g_small_t_max.store(t_max, std::memory_order_relaxed);
+    return RMSN_OK;
+}
+
+int64_t rmsn_small_t_max(void) { return g_small_t_max.load(std::memory_order_relaxed); }
+
 int rmsn_device_status(rmsn_stream_t stream, unsigned* flags) {
     if (!flags) return RMSN_ERR_INVALID_ARG;
     int dev = 0;
@@ -389,6 +404,9 @@ int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w
     int st = plan_current(RMSN_OP_BWD, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
     if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (small_t(deterministic, T))
+        return from_cuda(rmsn::launch_bwd_small(dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
+                                                compensated, s));
     return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                       deterministic, compensated,
                                       static_cast<float*>(workspace), s));
@@ -434,6 +452,9 @@ int rmsnorm_bwd_residual(const void* dy, const void* h, int x_dtype, const void*
     int st = plan_current(RMSN_OP_BWD_RESIDUAL, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
     if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (small_t(deterministic, T))
+        return from_cuda(rmsn::launch_bwd_small(dy, h, x_dtype, w, w_dtype, rstd, dx_total, dw, T,
+                                                H, compensated, s, g_residual));
     return from_cuda(rmsn::launch_bwd(L, dy, h, x_dtype, w, w_dtype, rstd, dx_total, dw, T, H,
                                       deterministic, compensated,
                                       static_cast<float*>(workspace), s, g_residual));
@@ -511,6 +532,9 @@ extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, int x_dtype, c
     }
     void* scratch = noalloc_scratch(dev);
     if (!scratch) return RMSN_ERR_CUDA;
+    if (small_t(1, T))  // the one-launch small-T kernel needs no scratch
+        return from_cuda(rmsn::launch_bwd_small(dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
+                                                compensated, s));
     return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                       /*deterministic=*/1, compensated,
                                       static_cast<float*>(scratch), s));

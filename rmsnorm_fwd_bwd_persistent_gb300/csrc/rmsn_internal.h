@@ -42,6 +42,12 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
                        int deterministic, int compensated, float* ws, cudaStream_t s,
                        const void* g_residual = nullptr);
 
+// Deterministic backward for small T in one launch (row tasks for dx, column tasks for dw;
+// no workspace).  g_residual selects the residual variant.
+cudaError_t launch_bwd_small(const void* dy, const void* x, int x_dt, const void* w, int w_dt,
+                             const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
+                             int compensated, cudaStream_t s, const void* g_residual = nullptr);
+
 cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const void* w,
                          uint8_t* q, float* block_scale, int64_t scale_ld, void* normed,
                          int64_t T, int64_t H, float eps, cudaStream_t s);
