@@ -294,6 +294,43 @@ def time_extra(step: Step, steps: int, warmup: int):
     return out
 
 
+def time_graph(step: Step, steps: int):
+    """The step (three ops, each after an L2 flush) captured once in a CUDA graph and
+    replayed: per-step time of the ops = (replays of [flush, op] x 3 - replays of the three
+    flushes alone) / replays, with CUDA events around each batch of replays."""
+    def ops():
+        for op in Step.OPS:
+            step.flush()
+            step.run_op(op)
+
+    def flushes():
+        for _ in Step.OPS:
+            step.flush()
+
+    graphs = []
+    for fn in (ops, flushes):
+        fn()  # every one-time set-up happens before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    times = []
+    for g in graphs:
+        for _ in range(3):
+            g.replay()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(steps):
+            g.replay()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e) / steps)
+    return {"ms_per_step": times[0] - times[1], "replays": steps,
+            "note": "ops of one step from CUDA-graph replay, flush time subtracted"}
+
+
 def time_small_t(dev, steps: int, warmup: int):
     """The determinism sweep's T=65 rows (bf16 x/dy, fp32 w) through the deterministic
     backward, on the one-launch small-T route and on the strip route; mean us per call,
@@ -489,6 +526,7 @@ def run_ours(args, world, rank, local):
 
     extra = time_extra(step, min(args.steps, 200), 3)
     small = time_small_t(dev, min(args.steps, 200), 3)
+    graph = time_graph(step, min(args.steps, 200))
     e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
     e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
@@ -526,6 +564,8 @@ def run_ours(args, world, rank, local):
                      "peak_source": peak_src},
         "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
         "bwd_small_t_route": small,
+        "graph_replay": dict(graph, eager_ms_per_step=max_ms,
+                             gbs=step_bytes / (graph["ms_per_step"] * 1e-3) / 1e9),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
