@@ -373,35 +373,65 @@ def time_small_t(dev, steps: int, warmup: int):
 
 def time_e2e(step: Step, steps: int, warmup: int):
     """The same step through the public API from pinned host buffers: every step copies
-    its inputs host->device, runs the three ops and copies every output device->host."""
+    all its inputs host->device, runs the three ops and copies every output device->host.
+    Steps are pipelined over two sets of device buffers and three streams (inputs of step
+    i+1 and outputs of step i-1 move while step i computes); events order each set's
+    reuse.  Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
     dev = step.x.device
-    ins = {k: getattr(step, k) for k in ("x", "dy", "w", "fx", "fres", "fw")}
-    outs = {k: getattr(step, k) for k in ("y", "rstd", "dx", "dw", "q", "scale", "normed", "fres")}
-    h_in = {k: v.cpu().pin_memory() for k, v in ins.items()}
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    in_names = ("x", "dy", "w", "fx", "fres", "fw")
+    out_names = ("y", "rstd", "dx", "dw", "q", "scale", "normed", "fres")
+    h_in = {k: getattr(step, k).cpu().pin_memory() for k in in_names}
+    sets = []
+    for _ in range(2):
+        d = {k: torch.empty_like(getattr(step, k)) for k in set(in_names) | set(out_names)}
+        d["ws"] = torch.empty_like(step.ws)
+        d["h_out"] = {k: torch.empty(getattr(step, k).shape, dtype=getattr(step, k).dtype,
+                                     pin_memory=True) for k in out_names}
+        sets.append(d)
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    d2h = sum(v.numel() * v.element_size() for v in sets[0]["h_out"].values())
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    rmsn = step.rmsn
 
-    def one():
-        for k, v in ins.items():
-            v.copy_(h_in[k], non_blocking=True)
-        step.fwd()
-        step.bwd()
-        step.fused()
-        for k, v in outs.items():
-            h_out[k].copy_(v, non_blocking=True)
+    def one(i, ev):
+        d = sets[i % 2]
+        e_free = ev.get(("out", i - 2))      # set reusable once step i-2's outputs left
+        with torch.cuda.stream(s_in):
+            if e_free is not None:
+                s_in.wait_event(e_free)
+            for k in in_names:
+                d[k].copy_(h_in[k], non_blocking=True)
+            ev[("in", i)] = torch.cuda.Event()
+            ev[("in", i)].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev[("in", i)])
+            rmsn.rmsnorm_fwd(d["x"], d["w"], step.eps, y=d["y"], rstd=d["rstd"])
+            rmsn.rmsnorm_bwd(d["dy"], d["x"], d["w"], d["rstd"], True, False, d["ws"], d["dx"], d["dw"])
+            rmsn.fused_add_rmsnorm_fp8_block_quant(d["fx"], d["fres"], d["fw"], step.eps, d["q"],
+                                                   d["scale"], d["normed"])
+            ev[("comp", i)] = torch.cuda.Event()
+            ev[("comp", i)].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev[("comp", i)])
+            for k in out_names:
+                d["h_out"][k].copy_(d[k], non_blocking=True)
+            ev[("out", i)] = torch.cuda.Event()
+            ev[("out", i)].record(s_out)
 
-    for _ in range(warmup):
-        one()
+    ev = {}
+    for i in range(warmup):
+        one(i, ev)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        one()
-    e.record()
-    e.synchronize()
+    ev = {}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for i in range(steps):
+        one(i, ev)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
+    t1.synchronize()
     del dev
-    return s.elapsed_time(e) / steps, h2d, d2h
+    return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
 # --------------------------------------------------------------------- oracle legs
