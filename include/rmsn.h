@@ -104,8 +104,9 @@ int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y,
  * (SM count x CTAs per SM) chunks and never more than T.  The value returned for (T, H)
  * is an upper bound for every T' <= T with the same H and device, so one buffer can be
  * reused across calls.  `device` is a CUDA device ordinal (its SM count decides the
- * number of chunks); `compensated` does not change the size.  Returns 0 for T <= 0, for an unsupported H, or when the
- * device cannot be queried.
+ * number of chunks); `compensated` does not change the size.  The same bound serves
+ * rmsnorm_bwd_residual.  Returns 0 for T <= 0, for an unsupported H, or when the device
+ * cannot be queried.
  * ---------------------------------------------------------------------------------- */
 size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int device);
 
@@ -129,15 +130,18 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *   deterministic  != 0: each row chunk's partial goes to the workspace and a second
  *         kernel sums the partials per column in a fixed order; dw is bitwise
  *         reproducible and a function of (T, H, dtypes, compensated, the device, the
- *         library build and the launch policy) only.
+ *         library build and the launch policy) only.  For T <= rmsn_small_t_max() (256
+ *         by default) one kernel does the whole backward instead, with dw summed over
+ *         all rows per column slab in a fixed order (see rmsn_set_small_t_max).
  *         == 0: dw is zeroed and the chunk partials are added to it with FP32 atomics
  *         (no second kernel, no workspace; bits may differ from run to run, and the
  *         cross-chunk sum is plain FP32, so above T ~ 65536 single elements can leave
  *         the atol 1e-4 + rtol 1e-4 budget).
  *   compensated  != 0: each thread adds every product dy*xhat to an FP32 (high, low)
  *         pair with the error-free TwoSum transformation.
- *         == 0: each thread sums the products of 4 consecutive rows with FMAs and adds
- *         each such block sum to the (high, low) pair with TwoSum (blocked FP32 sums).
+ *         == 0: each thread sums the products of the two rows of each row pair it
+ *         processes with one FMA and adds that block sum to the (high, low) pair with
+ *         TwoSum (blocked FP32 sums, blocks of two rows).
  *         In both cases the chunk partials are (high, low) pairs and the column
  *         reduction merges them with TwoSum; dw = high + low rounded once.
  *   workspace, workspace_bytes  device scratch of at least
@@ -227,8 +231,7 @@ int rmsnorm_fwd_residual(const void* x, const void* residual, int x_dtype, const
  *   dx_total    device [T, H], h's dtype (written); it may alias dy or g_residual exactly
  * The workspace and its size rule are those of rmsnorm_bwd (rmsnorm_bwd_workspace_bytes
  * covers both calls); the deterministic, compensated and error behaviour is the same.
- * Shapes: as rmsnorm_bwd, and H <= 14400 for bf16 (each ring stage holds three rows);
- * larger H returns RMSN_ERR_UNSUPPORTED_SHAPE.
+ * Shapes: as rmsnorm_bwd.
  * ---------------------------------------------------------------------------------- */
 int rmsnorm_bwd_residual(const void* dy, const void* h, int x_dtype, const void* w, int w_dtype,
                          const float* rstd, const void* g_residual, void* dx_total, float* dw,

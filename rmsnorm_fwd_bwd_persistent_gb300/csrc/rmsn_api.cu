@@ -43,7 +43,7 @@ constexpr Policy kDefaultPolicy[kOps] = {
     {0, 2, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
     {0, 3, 2, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM
     {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
-    {0, 2, 4, 2, 8},   // residual backward: as the backward, three rows per stage
+    {0, 2, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
 };
 Policy g_policy[kOps] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2],
                          kDefaultPolicy[3], kDefaultPolicy[4]};
@@ -154,8 +154,9 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
 
     const int64_t row_bytes = H * esize(x_dt);
     const int64_t row_pad = cdiv(row_bytes, 128) * 128;
-    // rows per stage: x; x and residual; x and dy; x, dy and g_residual
-    const int rows = op == RMSN_OP_FWD ? 1 : op == RMSN_OP_BWD_RESIDUAL ? 3 : 2;
+    // rows per stage: x; x and residual; x and dy (both backwards; the residual backward
+    // reads g_residual from global memory)
+    const int rows = op == RMSN_OP_FWD ? 1 : 2;
     const int64_t stage_bytes = rows * row_pad;
     const int64_t w_bytes = H * 4;  // w is staged in shared memory as FP32
     const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
@@ -274,7 +275,7 @@ const char* rmsn_status_string(int status) {
         case RMSN_ERR_UNSUPPORTED_SHAPE:
             return "unsupported shape (H must be a positive multiple of the 16-byte vector, "
                    "at most 16384; the fused quant needs H % 128 == 0; the fp32 backward "
-                   "at most 8192; the bf16 residual backward at most 14400)";
+                   "at most 8192)";
         case RMSN_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
         case RMSN_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than rmsnorm_bwd_workspace_bytes";
         case RMSN_ERR_CUDA: return "CUDA error (launch or runtime call failed)";

@@ -24,9 +24,10 @@
 //   compensated = 0: the two terms of a row pair are summed with one FMA and the block
 //                    sum is added with TwoSum ("blocked FP32 sums", blocks of two rows).
 // Residual variant (RES; FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward and
-// API: the backward adds g_residual into the dx it returns, dx_total): the stage holds the
-// x (= h_new), dy and g_residual rows; pass 2 adds g_residual to the FP32 dx before the
-// one rounding to x's dtype.
+// API: the backward adds g_residual into the dx it returns, dx_total): the feeding thread
+// prefetches each row's g_residual into L2 (bulk prefetch) when it issues the row's copies,
+// and pass 2 reads it from global memory and adds it to the FP32 dx before the one
+// rounding to x's dtype.
 // At the end of the strip the CTA writes its (high, low) partial row to the workspace
 // (deterministic mode) or adds high+low to dw with FP32 atomics.
 //
@@ -76,8 +77,7 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     const int64_t b = blockIdx.x;
     const int64_t nrows = (a.T - 1 - b) / nch + 1;  // rows b, b + n, ... below T
     // stage = [x row | dy row (| g_residual row)], each padded to the same size
-    const uint32_t dy_off = RES ? a.stage_bytes / 3 : a.stage_bytes / 2;
-    const uint32_t g_off = 2 * dy_off;
+    const uint32_t dy_off = a.stage_bytes / 2;  // stage = [x row | dy row], each padded
     stage_weights_f32<VEC>(static_cast<const TW*>(a.w), a.H, smem + kRingHeader);
     ring_init(ring, nw);
 
@@ -107,12 +107,11 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
             }
             const int64_t off = (b + issued * nch) * (int64_t)a.row_bytes;
             uint8_t* dst = ring.stage(in.s);
-            mbar_arrive_expect_tx(&ring.full[in.s], (RES ? 3 : 2) * a.row_bytes);
+            mbar_arrive_expect_tx(&ring.full[in.s], 2 * a.row_bytes);
             bulk_load(dst, X + off, a.row_bytes, &ring.full[in.s]);
             bulk_load(dst + dy_off, DY + off, a.row_bytes, &ring.full[in.s]);
-            if constexpr (RES)
-                bulk_load(dst + g_off, static_cast<const uint8_t*>(a.gres) + off, a.row_bytes,
-                          &ring.full[in.s]);
+            if constexpr (RES)  // g_residual is read in pass 2 from global memory: bring it to L2
+                bulk_prefetch_l2(static_cast<const uint8_t*>(a.gres) + off, a.row_bytes);
         }
     };
     issue_below(ring.stages);
@@ -134,7 +133,7 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
     // KEEP: pass 1 keeps the pair's x and dy vectors in registers for pass 2, so both
     // stages are released before the barrier and the whole ring can be in flight during
     // pass 2.  Otherwise (long rows) pass 2 reads them from the stages again.
-    constexpr bool KEEP = NCH <= 2 && !RES;
+    constexpr bool KEEP = NCH <= 2;
     uint4 xr[2][NCH], dr[2][NCH];
 
     // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row
@@ -200,6 +199,8 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
         const f2 rsb = f2_splat(rs1), ncb = f2_splat(-c1);
         TX* dx0 = DX + row0 * H;
         TX* dx1 = dx0 + nch * H;
+        const uint4* gr0 = RES ? reinterpret_cast<const uint4*>(static_cast<const TX*>(a.gres) + row0 * H)
+                               : nullptr;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int v = c * NC + t;
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
                 for (int i = 0; i < NP; ++i) o[i] = mul2(rsa, fma2(xp[i], nca, mul2(dp[i], wp[i])));
                 if constexpr (RES) {  // dx_total = dx + g_residual, rounded once
-                    Pairs<TX>::get(lds128(s0 + g_off + (size_t)v * 16), xp);
+                    Pairs<TX>::get(ldg_stream(gr0 + v), xp);
 #pragma unroll
                     for (int i = 0; i < NP; ++i) o[i] = add2(o[i], xp[i]);
                 }
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
                     for (int i = 0; i < NP; ++i) o[i] = mul2(rsb, fma2(xp[i], ncb, mul2(dp[i], wp[i])));
                     if constexpr (RES) {
-                        Pairs<TX>::get(lds128(s1 + g_off + (size_t)v * 16), xp);
+                        Pairs<TX>::get(ldg_stream(gr0 + nch * nvec + v), xp);
 #pragma unroll
                         for (int i = 0; i < NP; ++i) o[i] = add2(o[i], xp[i]);
                     }
