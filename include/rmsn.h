@@ -316,6 +316,15 @@ int64_t rmsn_small_t_max(void);
  * ---------------------------------------------------------------------------------- */
 int rmsn_device_status(rmsn_stream_t stream, unsigned* flags);
 
+/* Self-test of the bounded waits (no counterpart on the pages; it checks this library's
+ * own failure path): enqueues on `stream` one CTA that waits on an mbarrier nobody will
+ * complete, with a limit of `limit_ns` (1 .. 10^9), so the wait runs out and sets bit 0 of
+ * the current device's error word, as a pipeline wait that never sees its row would.  No
+ * copy is in flight and nothing else waits on it.  A following rmsn_device_status returns
+ * RMSN_ERR_DEVICE_TIMEOUT with bit 0 set, and clears the word.  Returns RMSN_OK once the
+ * kernel is enqueued, RMSN_ERR_INVALID_ARG for a limit out of range. */
+int rmsn_selftest_wait_timeout(uint64_t limit_ns, rmsn_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * rmsnorm_bwd_noalloc -- the deterministic rmsnorm_bwd for callers that cannot allocate.
  *

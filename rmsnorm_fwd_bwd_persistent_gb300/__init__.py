@@ -20,7 +20,7 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "rmsnorm_fwd_residual", "rmsnorm_bwd_residual",
     "fused_add_rmsnorm_fp8_block_quant", "rmsn_status_string", "rmsn_plan", "rmsn_set_policy",
-    "rmsn_device_status", "rmsn_set_small_t_max", "rmsn_small_t_max",
+    "rmsn_device_status", "rmsn_set_small_t_max", "rmsn_small_t_max", "rmsn_selftest_wait_timeout",
     "OP_FWD", "OP_BWD", "OP_FUSED_QUANT", "OP_FWD_RESIDUAL", "OP_BWD_RESIDUAL",
 ]
 
@@ -85,6 +85,8 @@ def load_library():
         L.rmsn_set_small_t_max.argtypes = [_i64]
         L.rmsn_small_t_max.restype = _i64
         L.rmsn_small_t_max.argtypes = []
+        L.rmsn_selftest_wait_timeout.restype = ctypes.c_int
+        L.rmsn_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
         L.rmsnorm_fwd_residual.restype = ctypes.c_int
         L.rmsnorm_fwd_residual.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp,
                                            _vp, _i64, _i64, ctypes.c_float, _vp]
@@ -337,6 +339,14 @@ def rmsn_set_small_t_max(t_max: int):
 
 def rmsn_small_t_max() -> int:
     return int(load_library().rmsn_small_t_max())
+
+
+def rmsn_selftest_wait_timeout(limit_ns: int = 2_000_000):
+    """Enqueues one CTA whose bounded wait runs out after limit_ns (no copy in flight);
+    the next rmsn_device_status reports the timeout."""
+    st = load_library().rmsn_selftest_wait_timeout(
+        int(limit_ns), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    _check(st, "rmsn_selftest_wait_timeout")
 
 
 def rmsn_device_status(device: int | torch.device | None = None) -> int:

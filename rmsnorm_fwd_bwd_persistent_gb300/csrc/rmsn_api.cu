@@ -333,6 +333,18 @@ int rmsn_set_small_t_max(int64_t t_max) {
 
 int64_t rmsn_small_t_max(void) { return g_small_t_max.load(std::memory_order_relaxed); }
 
+int rmsn_selftest_wait_timeout(uint64_t limit_ns, rmsn_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > kWaitLimitNs) return RMSN_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSN_ERR_CUDA;
+    }
+    unsigned* w = error_word(dev);
+    if (!w) return RMSN_ERR_CUDA;
+    return from_cuda(rmsn::launch_wait_selftest(w, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int rmsn_device_status(rmsn_stream_t stream, unsigned* flags) {
     if (!flags) return RMSN_ERR_INVALID_ARG;
     int dev = 0;

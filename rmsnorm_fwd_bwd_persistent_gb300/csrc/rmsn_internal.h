@@ -42,6 +42,10 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
                        int deterministic, int compensated, float* ws, cudaStream_t s,
                        const void* g_residual = nullptr);
 
+// One CTA that waits on an mbarrier nobody arrives at, with the given limit (self-test of
+// the bounded wait; sets ERR_WAIT_FULL in *err).
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t s);
+
 // Deterministic backward for small T in one launch (row tasks for dx, column tasks for dw;
 // no workspace).  g_residual selects the residual variant.
 cudaError_t launch_bwd_small(const void* dy, const void* x, int x_dt, const void* w, int w_dt,
