@@ -214,6 +214,22 @@ int plan_current(int op, int64_t T, int64_t H, int x_dt, int w_dt, Launch* L, in
 
 namespace rmsn {
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that expects an arrival
+// nobody makes (no copy is in flight), gives up after `limit_ns`, and reports it through
+// the error word exactly as a pipeline wait does.
+__global__ void rmsn_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait(&bar, 0u, limit_ns)) atomicOr(err, ERR_WAIT_FULL);
+}
+
+cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t s) {
+    rmsn_wait_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t fit_grid(const void* kernel, const Launch& L, int threads, int64_t* grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -171,22 +171,6 @@ static cudaError_t dispatch(const Launch& L, const FwdArgs& a, cudaStream_t s) {
     }
 }
 
-// Self-test of the bounded wait: one thread waits on an mbarrier that expects an arrival
-// nobody makes (no copy is in flight), gives up after `limit_ns`, and reports it through
-// the error word exactly as a pipeline wait does.
-__global__ void rmsn_wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
-    __shared__ __align__(8) uint64_t bar;
-    if (threadIdx.x != 0) return;
-    mbar_init(&bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (!mbar_wait(&bar, 0u, limit_ns)) atomicOr(err, ERR_WAIT_FULL);
-}
-
-cudaError_t launch_wait_selftest(unsigned* err, uint64_t limit_ns, cudaStream_t s) {
-    rmsn_wait_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_fwd(const Launch& L, const void* x, int x_dt, const void* w, int w_dt,
                        void* y, float* rstd, int64_t T, int64_t H, float eps, cudaStream_t s,
                        const void* residual, void* h_new) {
