@@ -26,11 +26,12 @@ constexpr int64_t kDefaultSmemPerSm = 233472;   // 228 KiB on sm_100 / sm_103
 constexpr int64_t kDefaultSmemPerCta = 232448;  // 227 KiB opt-in maximum per CTA
 constexpr int64_t kSmemReservedPerCta = 1024;   // set aside by the driver for each CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every pipeline wait gives up after 1 s
+constexpr int kWarpsPerSm = 16;  // the backward's consumer warps per SM (measured best on GB300)
 
 // ------------------------------------------------------------------ policy defaults
 struct Policy {
     int consumer_warps;  // 0: derived from H (target_nch vectors per lane)
-    int ctas_per_sm;
+    int ctas_per_sm;     // 0: kWarpsPerSm / consumer warps (backward)
     int max_stages;
     int target_nch;
     int max_nch;
@@ -40,10 +41,10 @@ struct Policy {
 constexpr int kOps = 5;
 constexpr Policy kDefaultPolicy[kOps] = {
     {0, 4, 2, 4, 16},  // forward: small CTAs, 4 per SM, two stages each
-    {0, 2, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, accumulators in registers
+    {0, 0, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, 16 warps per SM
     {0, 3, 2, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM
     {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
-    {0, 2, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
+    {0, 0, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
 };
 Policy g_policy[kOps] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2],
                          kDefaultPolicy[3], kDefaultPolicy[4]};
@@ -160,7 +161,8 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     const int64_t stage_bytes = rows * row_pad;
     const int64_t w_bytes = H * 4;  // w is staged in shared memory as FP32
     const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
-    int cps = P.ctas_per_sm;
+    // CTAs per SM: the policy's, or enough CTAs for kWarpsPerSm consumer warps per SM
+    int cps = P.ctas_per_sm > 0 ? P.ctas_per_sm : (nw >= kWarpsPerSm ? 1 : kWarpsPerSm / nw);
     auto stages_for = [&](int c) -> int64_t {
         int64_t share = smem_sm / c - kSmemReservedPerCta;
         if (share > smem_cta) share = smem_cta;
@@ -403,13 +405,19 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
     if (T <= 0 || H <= 0 || H > RMSN_MAX_H || H % 4 != 0) return 0;
     const DevProps* p = props_of(device);
     if (!p) return 0;
-    // The chunk count never exceeds min(T, SMs * CTAs per SM) whatever the dtypes, and
-    // grows with T, so this bounds every call with T' <= T.
-    // (rmsnorm_bwd and rmsnorm_bwd_residual alike: the larger of their CTAs per SM)
-    const int cps = std::max(policy(RMSN_OP_BWD).ctas_per_sm, policy(RMSN_OP_BWD_RESIDUAL).ctas_per_sm);
-    int64_t chunks = (int64_t)p->sms * cps;
-    if (chunks > T) chunks = T;
-    return (size_t)(chunks * H * 4 * 2);
+    // The largest workspace any plan of rmsnorm_bwd or rmsnorm_bwd_residual needs for this
+    // (T, H) over the dtype pairs; each grows with T (min(T, SMs x CTAs per SM) chunks), so
+    // this bounds every call with T' <= T.
+    int64_t best = 0;
+    for (int op : {(int)RMSN_OP_BWD, (int)RMSN_OP_BWD_RESIDUAL})
+        for (int xd : {(int)RMSN_F32, (int)RMSN_BF16})
+            for (int wd : {(int)RMSN_F32, (int)RMSN_BF16}) {
+                Launch L{};
+                int64_t ws = 0;
+                if (plan(op, T, H, xd, wd, p->sms, p->smem_sm, p->smem_cta, &L, &ws) == RMSN_OK)
+                    best = std::max(best, ws);
+            }
+    return (size_t)best;
 }
 
 int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w_dtype,

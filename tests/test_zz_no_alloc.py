@@ -55,7 +55,7 @@ def test_noalloc_matches_workspace_backward_twice(T, H, wd, compensated):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    T, H = 4096, 16384  # needs 8 * H * min(T, 2 * SMs) bytes, well above 16 MiB
+    T, H = 4096, 16384  # needs 8 * H * min(T, SMs * CTAs per SM) bytes, well above 16 MiB
     x = torch.zeros(T, H, device="cuda", dtype=torch.bfloat16)
     w = torch.ones(H, device="cuda", dtype=torch.bfloat16)
     rstd = torch.ones(T, device="cuda")
