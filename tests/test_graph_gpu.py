@@ -31,18 +31,24 @@ def test_graph_replay_matches_eager(T):
         rmsn.rmsnorm_bwd(dy, x, w, o["rstd"], True, False, ws, o["dx"], o["dw"])
         rmsn.fused_add_rmsnorm_fp8_block_quant(fx, o["res"], fw, c.eps, o["q"], o["sc"], o["nm"])
 
-    eager = outputs()
-    run(eager)
+    run(outputs())  # every one-time set-up happens before the capture
     torch.cuda.synchronize()
     g_out = outputs()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         run(g_out)
-    for _ in range(2):  # the fused op updates residual in place: restore it before a replay
-        g_out["res"].copy_(fres0)
+    for rep in range(3):
+        if rep:  # new data in the same buffers: a replay must not reuse anything stale
+            gen = torch.Generator(device=DEV).manual_seed(100 + rep)
+            x.copy_(torch.randn(x.shape, generator=gen, device=DEV).to(x.dtype))
+            dy.copy_(torch.randn(dy.shape, generator=gen, device=DEV).to(dy.dtype))
+            fx.copy_(torch.randn(fx.shape, generator=gen, device=DEV).to(fx.dtype))
+        eager = outputs()
+        run(eager)
+        g_out["res"].copy_(fres0)  # the fused op updates residual in place
         graph.replay()
         torch.cuda.synchronize()
         for k in eager:
             a, b = eager[k], g_out[k]
-            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), k
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (rep, k)
     assert rmsn.rmsn_device_status() == 0
