@@ -294,6 +294,37 @@ def time_extra(step: Step, steps: int, warmup: int):
     return out
 
 
+def time_long_strip(dev, steps: int, warmup: int, peak: float):
+    """The deterministic backward over a long strip (T=65536, H=4096 bf16: 216 rows per CTA
+    instead of 27), where the per-call fixed costs amortise; same protocol (L2 flushed before
+    each call, CUDA events around it)."""
+    import dataclasses
+    import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+    c = dataclasses.replace(wl.MAIN_BF16, T=65536)
+    x, dy, w = wl.fwd_bwd_inputs(c, dev, 3)
+    _, rstd = rmsn.rmsnorm_fwd(x, w, c.eps)
+    dx, dw = torch.empty_like(x), torch.empty(c.H, device=dev)
+    ws = torch.empty(rmsn.rmsnorm_bwd_workspace_bytes(c.T, c.H, False, dev), device=dev,
+                     dtype=torch.uint8)
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    rd = flush.view(torch.float32)[: (FLUSH_BYTES // 2) // 4]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(warmup + steps):
+        flush.zero_()
+        rd.sum()
+        if i >= warmup:
+            ev[i - warmup][0].record()
+        rmsn.rmsnorm_bwd(dy, x, w, rstd, True, False, ws, dx, dw)
+        if i >= warmup:
+            ev[i - warmup][1].record()
+    torch.cuda.synchronize()
+    us = statistics.mean(s.elapsed_time(e) for s, e in ev) * 1e3
+    by = wl.bwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype)
+    return {"workload": "deterministic bwd, T=65536 H=4096 bf16", "us_mean": us,
+            "gbs": by / (us * 1e-6) / 1e9, "frac": by / (us * 1e-6) / 1e9 / peak, "bytes": by}
+
+
 def time_graph(step: Step, steps: int):
     """The step (three ops, each after an L2 flush) captured once in a CUDA graph and
     replayed: per-step time of the ops = (replays of [flush, op] x 3 - replays of the three
@@ -557,6 +588,7 @@ def run_ours(args, world, rank, local):
     extra = time_extra(step, min(args.steps, 200), 3)
     small = time_small_t(dev, min(args.steps, 200), 3)
     graph = time_graph(step, min(args.steps, 200))
+    long_strip = time_long_strip(dev, min(args.steps, 100), 3, peak)
     e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
     e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
@@ -594,6 +626,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": peak_src},
         "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
         "bwd_small_t_route": small,
+        "bwd_long_strip": long_strip,
         "graph_replay": dict(graph, eager_ms_per_step=max_ms,
                              gbs=step_bytes / (graph["ms_per_step"] * 1e-3) / 1e9),
         "cpu_baseline": cpu,
