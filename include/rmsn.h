@@ -283,8 +283,8 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
               int sm_count, rmsn_plan_t* out);
 
 /* Tuning hook for benchmarks: overrides the consumer warps per CTA (a power of two
- * <= 8), the CTAs per SM and the maximum ring depth of one op for the whole process
- * (0 keeps a default).  The backward's chunk count, and so its dw bits, follow the CTAs
+ * <= 8; <= 16 for the two backward ops), the CTAs per SM and the maximum ring depth of
+ * one op for the whole process (0 keeps a default).  The backward's chunk count, and so its dw bits, follow the CTAs
  * per SM; rmsnorm_bwd_workspace_bytes reflects the current setting.  Changing it while
  * calls are in flight on other host threads is a race.  Returns RMSN_ERR_INVALID_ARG for
  * values out of range (then nothing changes). */
@@ -342,8 +342,9 @@ int rmsn_selftest_wait_timeout(uint64_t limit_ns, rmsn_stream_t stream);
  * same kernels, so the same dx and, for the same device, dw).  The caller still provides
  * dy, x, w, rstd, dx and dw.
  *   - Returns RMSN_ERR_SCRATCH_LIMIT (nothing enqueued) when the call would need more than
- *     RMSN_NOALLOC_SCRATCH_BYTES of scratch, i.e. when 8 * H * min(T, SMs * 2) exceeds it
- *     (on a 152-SM GB300: H <= 6144 always fits; H = 8192 fits up to T = 256).
+ *     RMSN_NOALLOC_SCRATCH_BYTES of scratch, i.e. when 8 * H * (row chunks) exceeds it,
+ *     the chunks being min(T, SMs * CTAs per SM) as rmsn_plan reports them (on a 152-SM
+ *     GB300 with bf16 x: H <= 8192 always fits; H = 16384 fits up to T = 128).
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
  *   - All calls in the process share the one array.  Every call writes all the scratch it

@@ -123,7 +123,8 @@ int pick_nch(const int (&set)[N], int64_t need) {
 }
 
 // The launch plan of one call.  Consumer warps: the smallest power of two (<= 8) whose
-// lanes hold about `target_nch` 16-byte vectors of a row each; the chunk variant is the
+// lanes hold about `target_nch` 16-byte vectors of a row each (the backward: 16 for rows
+// of at least 512 * target_nch vectors); the chunk variant is the
 // smallest compiled count that covers the row.  Shared memory per CTA: the ring header,
 // the weight vector, and as many stages (<= max_stages) as the CTA's share of the SM
 // holds (the backward at least two); fewer CTAs per SM if a share cannot hold two stages.
@@ -138,6 +139,7 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     if (T < 0 || sms <= 0) return RMSN_ERR_INVALID_ARG;
     const int vec = 16 / esize(x_dt);
     if (H <= 0 || H > RMSN_MAX_H || H % vec != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
+    if (is_bwd && x_dt == RMSN_F32 && H > 8192) return RMSN_ERR_UNSUPPORTED_SHAPE;
     if (op == RMSN_OP_FUSED_QUANT && H % 128 != 0) return RMSN_ERR_UNSUPPORTED_SHAPE;
     const Policy P = policy(op);
     const int64_t nvec = H / vec;
@@ -145,6 +147,9 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     if (nw == 0) {
         nw = 1;
         while (nw < 8 && cdiv(nvec, 32 * nw) > P.target_nch) nw *= 2;
+        // backward rows that fill 16 warps at target_nch vectors per lane take 16 warps
+        // (one CTA per SM), so every lane keeps its share of a row pair in registers
+        if (is_bwd && nvec >= 16 * 32 * P.target_nch) nw = 16;
     }
     const int64_t need = cdiv(nvec, 32 * nw);
     int nch = 0;
@@ -329,7 +334,8 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
 
 int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages) {
     if (op < 0 || op >= kOps) return RMSN_ERR_INVALID_ARG;
-    if (consumer_warps < 0 || consumer_warps > 8 ||
+    const bool is_bwd = op == RMSN_OP_BWD || op == RMSN_OP_BWD_RESIDUAL;
+    if (consumer_warps < 0 || consumer_warps > (is_bwd ? 16 : 8) ||
         (consumer_warps & (consumer_warps - 1)) != 0)
         return RMSN_ERR_INVALID_ARG;
     if (ctas_per_sm < 0 || ctas_per_sm > 16 || max_stages < 0 || max_stages > 32)

@@ -67,7 +67,8 @@ struct BwdArgs {
 };
 
 template <typename TX, typename TW, int NCH, bool COMP, bool RES>
-__global__ void __launch_bounds__(256, 2) rmsnorm_bwd_kernel(BwdArgs a) {
+// 128 registers per thread: two CTAs of 8 warps or one of 16 per SM
+__global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
     const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);

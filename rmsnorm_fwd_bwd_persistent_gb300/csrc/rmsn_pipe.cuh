@@ -264,11 +264,13 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// True if any of the first nw (1, 2, 4 or 8) "gave up" bytes at f (8-byte aligned) is set.
+// True if any of the first nw (1, 2, 4, 8 or 16) "gave up" bytes at f (16-byte aligned) is
+// set.
 __device__ __forceinline__ bool any_gave_up(const uint8_t* f, int nw) {
-    const uint64_t all = *reinterpret_cast<const uint64_t*>(f);
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(f);
+    if (nw >= 16) return (w[0] | w[1]) != 0;
     const uint64_t mask = nw >= 8 ? ~0ull : ((1ull << (8 * nw)) - 1ull);
-    return (all & mask) != 0;
+    return (w[0] & mask) != 0;
 }
 
 // r[0] + r[1] + ... + r[nw-1], left to right, for nw in {1, 2, 4, 8} (r 16-byte aligned).
@@ -310,7 +312,7 @@ __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, i
 // lanes so that even lanes go on with v0 and odd lanes with v1; four more butterfly levels
 // among lanes of the same parity finish both warp sums (lane 0 holds v0's, lane 1 v1's).
 // Each warp posts its sums times m0 and m1 (rounded), and the posts are added in warp
-// order.  The order is fixed, so the bits depend only on the data.  nw is 1, 2, 4 or 8.
+// order.  The order is fixed, so the bits depend only on the data.  nw is 1, 2, 4, 8 or 16.
 __device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v1, float m0,
                                               float m1, bool ok, int nw, int parity) {
     const int lane = threadIdx.x & 31;
@@ -328,7 +330,17 @@ __device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v
     named_bar(1, nw * 32);
     const float4* r4 = reinterpret_cast<const float4*>(red);
     float s0, s1;
-    if (nw == 8) {
+    if (nw == 16) {
+        const float4 q0 = r4[0];
+        s0 = q0.x + q0.z;
+        s1 = q0.y + q0.w;
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            const float4 q = r4[i];
+            s0 = s0 + q.x + q.z;
+            s1 = s1 + q.y + q.w;
+        }
+    } else if (nw == 8) {
         const float4 a = r4[0], b = r4[1], c = r4[2], d = r4[3];
         s0 = a.x + a.z + b.x + b.z + c.x + c.z + d.x + d.z;
         s1 = a.y + a.w + b.y + b.w + c.y + c.w + d.y + d.w;

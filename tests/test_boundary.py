@@ -134,7 +134,7 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         assert p["vec_elems"] == vec
         assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
         producer = 0 if is_bwd else 32                              # bwd: thread 0 feeds the ring
-        assert p["threads"] == lanes + producer and p["threads"] <= 288
+        assert p["threads"] == lanes + producer and p["threads"] <= (512 if is_bwd else 288)
         assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
         row = H * (2 if xd == 1 else 4)
         rows = 1 if op == rmsn.OP_FWD else 2                        # rows per stage
