@@ -141,7 +141,10 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *         pair with the error-free TwoSum transformation.
  *         == 0: each thread sums the products of the two rows of each row pair it
  *         processes with one FMA and adds that block sum to the (high, low) pair with
- *         TwoSum (blocked FP32 sums, blocks of two rows).
+ *         TwoSum (blocked FP32 sums, blocks of two rows).  Where the kernel takes rows
+ *         one at a time (bf16 rows of about three 16-byte vectors per consumer lane,
+ *         e.g. H = 6144 with 8 consumer warps) the blocks are single rows, so both
+ *         settings give the same bits.
  *         In both cases the chunk partials are (high, low) pairs and the column
  *         reduction merges them with TwoSum; dw = high + low rounded once.
  *   workspace, workspace_bytes  device scratch of at least

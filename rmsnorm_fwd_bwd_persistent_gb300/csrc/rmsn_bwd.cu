@@ -66,7 +66,7 @@ struct BwdArgs {
     int atomic;
 };
 
-template <typename TX, typename TW, int NCH, bool COMP, bool RES>
+template <typename TX, typename TW, int NCH, bool COMP, bool RES, bool SINGLE>
 // 128 registers per thread: two CTAs of 8 warps or one of 16 per SM
 __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
     constexpr int VEC = Elem<TX>::VEC;
@@ -131,10 +131,15 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < NP; ++i) hi[c][i] = lo[c][i] = f2_splat(0.f);
 
-    // KEEP: pass 1 keeps the pair's x and dy vectors in registers for pass 2, so both
+    // SINGLE (bf16 rows of three vectors per lane, nearly all lanes full): rows go one at a
+    // time, so one row's x and dy fit in registers beside the accumulators (a pair's would
+    // not, in 128 registers), and every dw term is added with TwoSum whatever `compensated`
+    // says.
+    // KEEP: pass 1 keeps the rows' x and dy vectors in registers for pass 2, so their
     // stages are released before the barrier and the whole ring can be in flight during
     // pass 2.  Otherwise (long rows) pass 2 reads them from the stages again.
-    constexpr bool KEEP = NCH <= 2;
+    static_assert(!SINGLE || NCH == 3, "single-row mode is compiled for three vectors per lane");
+    constexpr bool KEEP = NCH <= 2 || SINGLE;
     uint4 xr[2][NCH], dr[2][NCH];
 
     // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row
@@ -240,7 +245,27 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
     // rstd of the next pair, loaded one pair ahead
     float rs_n0 = nrows > 0 ? __ldg(a.rstd + b) : 0.f;
     float rs_n1 = nrows > 1 ? __ldg(a.rstd + b + nch) : 0.f;
-    for (; k < nrows; k += 2, parity ^= 1) {
+    if constexpr (SINGLE) {
+        for (; k < nrows; ++k, parity ^= 1) {
+            const uint8_t* s0 = ring.stage(at0.s);
+            const int64_t row0 = b + k * nch;
+            const float rs0 = rs_n0;
+            if (k + 1 < nrows) rs_n0 = __ldg(a.rstd + row0 + nch);
+            float d0, d1;
+            issue_below(k + 1);
+            const bool ok = ring_wait_full(ring, at0, a.limit_ns, a.err);
+            pass1(std::false_type{}, s0, s0, ok, rs0, 0.f, d0, d1);
+            if (ok) ring_release(ring, at0);  // x and dy are in registers
+            if (!consumer_sum2(smem, d0, d1, __fmul_rn(rs0, __fmul_rn(rs0, invH)), 0.f, ok, nw,
+                               parity))
+                break;
+            // every warp has released this row's stage and the ones before it
+            issue_below(k + 1 + ring.stages);
+            pass2(std::false_type{}, row0, s0, s0, rs0, 0.f, d0, 0.f);
+            at0.advance(ring.stages);
+        }
+    }
+    for (; !SINGLE && k < nrows; k += 2, parity ^= 1) {
         Slot at1 = at0;
         at1.advance(ring.stages);
         const uint8_t* s0 = ring.stage(at0.s);
@@ -389,10 +414,10 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce_kernel(const float* __r
 }
 
 // Launches the main kernel; *grid receives the number of chunks it ran with.
-template <typename TX, typename TW, int NCH, bool COMP>
+template <typename TX, typename TW, int NCH, bool COMP, bool SINGLE = false>
 static cudaError_t run_main(const Launch& L, const BwdArgs& a, cudaStream_t s, int64_t* grid) {
-    auto k = a.gres ? rmsnorm_bwd_kernel<TX, TW, NCH, COMP, true>
-                    : rmsnorm_bwd_kernel<TX, TW, NCH, COMP, false>;
+    auto k = a.gres ? rmsnorm_bwd_kernel<TX, TW, NCH, COMP, true, SINGLE>
+                    : rmsnorm_bwd_kernel<TX, TW, NCH, COMP, false, SINGLE>;
     const int threads = L.nw * 32;  // consumer warps only
     cudaError_t e = fit_grid((const void*)k, L, threads, grid);
     if (e != cudaSuccess) return e;
@@ -405,7 +430,10 @@ static cudaError_t dispatch_nch(const Launch& L, const BwdArgs& a, cudaStream_t 
     switch (L.nch) {
         case 1: return run_main<TX, TW, 1, COMP>(L, a, s, g);
         case 2: return run_main<TX, TW, 2, COMP>(L, a, s, g);
-        case 3: return run_main<TX, TW, 3, COMP>(L, a, s, g);
+        case 3:
+            if constexpr (std::is_same<TX, __nv_bfloat16>::value)
+                if (L.single) return run_main<TX, TW, 3, COMP, true>(L, a, s, g);
+            return run_main<TX, TW, 3, COMP>(L, a, s, g);
         case 4: return run_main<TX, TW, 4, COMP>(L, a, s, g);
         case 6: return run_main<TX, TW, 6, COMP>(L, a, s, g);
         case 8: return run_main<TX, TW, 8, COMP>(L, a, s, g);

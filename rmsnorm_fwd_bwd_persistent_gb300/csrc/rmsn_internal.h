@@ -12,6 +12,7 @@ namespace rmsn {
 struct Launch {
     int nw;              // consumer warps per CTA
     int nch;             // 16-byte vectors per consumer lane per row (compile-time variant)
+    bool single;         // backward: rows one at a time (bf16 rows of three vectors per lane)
     int stages;          // ring depth
     int ctas_per_sm;     // CTAs per SM the grid is sized for
     int sms;             // multiprocessors of the device
