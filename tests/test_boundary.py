@@ -159,6 +159,21 @@ def test_plan_headline_geometry(lib):
     assert (q["consumer_warps"], q["chunks_per_lane"], q["ctas_per_sm"], q["stages"]) == (8, 2, 3, 2)
 
 
+@pytest.mark.parametrize("H,xd,geom", [
+    (1536, 1, (4, 2, 4)), (2048, 1, (4, 2, 4)), (4096, 1, (8, 2, 2)), (5120, 1, (8, 3, 2)),
+    (6144, 1, (8, 3, 2)), (8192, 1, (16, 2, 1)), (16384, 1, (16, 4, 1)),
+    (2048, 0, (8, 2, 2)), (4096, 0, (16, 2, 1)), (8192, 0, (16, 4, 1))])
+def test_plan_backward_geometry_by_row_length(lib, H, xd, geom):
+    # 16 consumer warps per SM: 4 CTAs of 4 warps, 2 of 8, or one of 16 for rows of at
+    # least 1024 16-byte vectors; the residual backward plans the same way
+    for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
+        p = rmsn.rmsn_plan(op, 65536, H, xd, 0)
+        assert (p["consumer_warps"], p["chunks_per_lane"], p["ctas_per_sm"]) == geom
+        assert p["consumer_warps"] * p["ctas_per_sm"] == 16
+        assert p["grid"] == SM * p["ctas_per_sm"]
+        assert p["workspace_bytes"] == 8 * H * p["grid"]
+
+
 def test_workspace_grows_with_t(lib):
     prev = 0
     for T in (1, 2, 3, 17, 100, 1000, 10 ** 4, 10 ** 5, 10 ** 6):

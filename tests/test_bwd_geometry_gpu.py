@@ -1,0 +1,67 @@
+"""GPU parity of the strip backward in every launch geometry its plan picks (T above the
+small-T route, so the deterministic calls run the strip kernel and the column reduce):
+4 CTAs of 4 warps, 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
+2 CTAs of 8 warps with rows one at a time (bf16, about three vectors per lane) and one CTA
+of 16 warps (rows of at least 1024 vectors), each against the FP64 oracle, with plain and
+TwoSum-compensated dW, for rmsnorm_bwd and rmsnorm_bwd_residual (FlashInfer PR #5741
+"cake_rmsnorm_train", Design/Backward; miles-ext-kernels PR #15, Changes #8848/#8849)."""
+import dataclasses
+
+import pytest
+import torch
+
+import _parity as P
+import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF, F32 = torch.bfloat16, torch.float32
+
+# (T, H, x dtype, w dtype, consumer warps, vectors per lane, CTAs per SM)
+GEOMETRIES = [
+    (1000, 2048, BF, F32, 4, 2, 4),
+    (777, 4096, BF, BF, 8, 2, 2),
+    (600, 5120, BF, F32, 8, 3, 2),
+    (600, 5632, BF, BF, 8, 3, 2),    # rows one at a time (third vector 3/4 full)
+    (555, 6144, BF, F32, 8, 3, 2),   # rows one at a time
+    (1000, 8192, BF, BF, 16, 2, 1),
+    (300, 16384, BF, F32, 16, 4, 1),
+    (513, 4096, F32, F32, 16, 2, 1),
+    (300, 8192, F32, BF, 16, 4, 1),
+]
+IDS = [f"T{g[0]}-H{g[1]}-{'bf16' if g[2] == BF else 'fp32'}" for g in GEOMETRIES]
+
+
+def _code(dt):
+    return 1 if dt == BF else 0
+
+
+@pytest.mark.parametrize("g", GEOMETRIES, ids=IDS)
+def test_bwd_geometry(g):
+    T, H, xd, wd, nw, nch, cps = g
+    p = rmsn.rmsn_plan(rmsn.OP_BWD, T, H, _code(xd), _code(wd),
+                       sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert (p["consumer_warps"], p["chunks_per_lane"], p["ctas_per_sm"]) == (nw, nch, cps)
+    assert T > rmsn.rmsn_small_t_max()
+    c = dataclasses.replace(wl.MAIN_BF16, T=T, H=H, x_dtype=xd, w_dtype=wd)
+    x, dy, w = wl.fwd_bwd_inputs(c, DEV, seed=T + H)
+    _, rstd = rmsn.rmsnorm_fwd(x, w, c.eps)
+    for comp in (False, True):
+        P.assert_ok(P.check_bwd(dy, x, w, rstd, compensated=comp), f"bwd {T}x{H} comp={comp}")
+    P.assert_ok(P.check_bwd(dy, x, w, rstd, deterministic=False), f"bwd fast {T}x{H}")
+
+
+@pytest.mark.parametrize("g", GEOMETRIES, ids=IDS)
+def test_bwd_residual_geometry(g):
+    T, H, xd, wd, nw, nch, cps = g
+    p = rmsn.rmsn_plan(rmsn.OP_BWD_RESIDUAL, T, H, _code(xd), _code(wd),
+                       sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert (p["consumer_warps"], p["chunks_per_lane"], p["ctas_per_sm"]) == (nw, nch, cps)
+    c = dataclasses.replace(wl.RESIDUAL_MAIN, T=T, H=H, x_dtype=xd, w_dtype=wd)
+    x, res, dy, gr, w = wl.residual_inputs(c, DEV, seed=T * 3 + H)
+    rf = P.check_fwd_residual(x, res, w, c.eps)
+    P.assert_ok(rf, f"fwd_residual {T}x{H}")
+    for comp in (False, True):
+        rb = P.check_bwd_residual(dy, rf["_h"], w, rf["_rstd_dev"], gr, compensated=comp)
+        P.assert_ok(rb, f"bwd_residual {T}x{H} comp={comp}")
