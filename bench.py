@@ -325,6 +325,70 @@ def time_long_strip(dev, steps: int, warmup: int, peak: float):
             "gbs": by / (us * 1e-6) / 1e9, "frac": by / (us * 1e-6) / 1e9 / peak, "bytes": by}
 
 
+def _mean_us(fn, steps: int, warmup: int, flush, rd) -> float:
+    """Mean CUDA-event time of fn in us, L2 flushed (outside the events) before each call."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(warmup + steps):
+        flush.zero_()
+        rd.sum()
+        if i >= warmup:
+            ev[i - warmup][0].record()
+        fn()
+        if i >= warmup:
+            ev[i - warmup][1].record()
+    torch.cuda.synchronize()
+    return statistics.mean(s.elapsed_time(e) for s, e in ev) * 1e3
+
+
+def time_configs(dev, steps: int, warmup: int, peak: float):
+    """Every other workload of the method, each alone, same protocol as the step's ops:
+    T=64 H=256 fp32 forward and backward; the fused add+norm+E4M3 quant at T=2048 H=4096;
+    the deterministic backward sweep (bf16 x/dy, fp32 w; T=65 is the small-T leg) and the
+    compensated backward at T=262144 H=5120."""
+    import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    rd = flush.view(torch.float32)[: (FLUSH_BYTES // 2) // 4]
+    out = {}
+
+    def rec(name, us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us_mean": us, "gbs": gbs, "frac": gbs / peak, "bytes": nbytes}
+
+    def bwd_case(c, compensated, n):
+        x, dy, w = wl.fwd_bwd_inputs(c, dev, 0)
+        _, rstd = rmsn.rmsnorm_fwd(x, w, c.eps)
+        dx, dw = torch.empty_like(x), torch.empty(c.H, device=dev)
+        ws = torch.empty(max(rmsn.rmsnorm_bwd_workspace_bytes(c.T, c.H, compensated, dev), 16),
+                         device=dev, dtype=torch.uint8)
+        us = _mean_us(lambda: rmsn.rmsnorm_bwd(dy, x, w, rstd, True, compensated, ws, dx, dw),
+                      n, warmup, flush, rd)
+        rec(c.name + ("_compensated" if compensated else ""), us,
+            wl.bwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype))
+
+    c = wl.SMALL_FP32
+    x, dy, w = wl.fwd_bwd_inputs(c, dev, 0)
+    y, rstd = torch.empty_like(x), torch.empty(c.T, device=dev)
+    rec(c.name + "_fwd", _mean_us(lambda: rmsn.rmsnorm_fwd(x, w, c.eps, y=y, rstd=rstd), steps,
+                                  warmup, flush, rd), wl.fwd_bytes(c.T, c.H, c.x_dtype, c.w_dtype))
+    bwd_case(c, False, steps)
+    f = wl.FUSED_QUANT
+    fx, fres, fw = wl.fused_inputs(f, dev, 0)
+    q = torch.empty(f.T, f.H, device=dev, dtype=torch.uint8)
+    sc = torch.empty(f.H // 128, wl.round_up(f.T, 4), device=dev)
+    nm = torch.empty_like(fx)
+    rec(f.name, _mean_us(lambda: rmsn.fused_add_rmsnorm_fp8_block_quant(fx, fres, fw, f.eps, q, sc,
+                                                                        nm),
+                         steps, warmup, flush, rd), wl.fused_quant_bytes(f.T, f.H))
+    for c in wl.DET_SWEEP:
+        if c.T > 65:
+            bwd_case(c, False, max(5, min(steps, 20)))
+            torch.cuda.empty_cache()
+    bwd_case(wl.TWOSUM_LARGE, True, max(5, min(steps, 10)))
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_graph(step: Step, steps: int):
     """The step (three ops, each after an L2 flush) captured once in a CUDA graph and
     replayed: per-step time of the ops = (replays of [flush, op] x 3 - replays of the three
@@ -589,6 +653,7 @@ def run_ours(args, world, rank, local):
     small = time_small_t(dev, min(args.steps, 200), 3)
     graph = time_graph(step, min(args.steps, 200))
     long_strip = time_long_strip(dev, min(args.steps, 100), 3, peak)
+    configs = time_configs(dev, min(args.steps, 100), 3, peak)
     e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, 3)
     e2e_ms_max, _ = aggregate(e2e_ms, step_bytes, world)
     e2e_value = total_bytes / (e2e_ms_max * 1e-3) / 1e9
@@ -627,6 +692,7 @@ def run_ours(args, world, rank, local):
         "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
         "bwd_small_t_route": small,
         "bwd_long_strip": long_strip,
+        "other_configs": configs,
         "graph_replay": dict(graph, eager_ms_per_step=max_ms,
                              gbs=step_bytes / (graph["ms_per_step"] * 1e-3) / 1e9),
         "cpu_baseline": cpu,

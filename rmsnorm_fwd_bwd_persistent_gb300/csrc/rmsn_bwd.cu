@@ -11,7 +11,8 @@
 // Main kernel: chunk c (= CTA c of a grid of n) owns the rows c, c + n, c + 2n, ...
 // (a static map, so the grid streams one window of consecutive rows at a time).  Consumer
 // thread 0 streams the x and dy rows into a shared-memory ring (there is no producer warp,
-// so each thread may hold more registers).  The consumer warps take the rows in pairs.
+// so each thread may hold more registers).  The consumer warps take the rows in pairs
+// (bf16 rows of three 16-byte vectors per lane one at a time: SINGLE below).
 // Pass 1 reads a pair from its two stages and forms p = dy * x per element (exact for bf16
 // inputs, one mixed-precision FMA each), the rows' d = sum(w * p), and adds the dw terms
 // dy * xhat = rstd * p into per-thread column accumulators that stay in registers for the
