@@ -142,8 +142,10 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         wpad = -(-(H * 4) // 128) * 128                           # w staged as FP32 in smem
         assert p["stages"] >= 1 and p["smem_bytes"] == 2048 + wpad + p["stages"] * stage
         assert p["ctas_per_sm"] * (p["smem_bytes"] + 1024) <= 233472  # fits the SM
-        if p["ctas_per_sm"] > 1 or is_bwd:
+        if is_bwd or (p["ctas_per_sm"] > 1 and op != rmsn.OP_FUSED_QUANT):
             assert p["stages"] >= 2                                 # bwd holds two rows
+        if op == rmsn.OP_FUSED_QUANT:
+            assert p["stages"] == 1                                 # one stage, 3 CTAs per SM
         if op == rmsn.OP_FUSED_QUANT:
             assert lanes % 16 == 0                                  # 16 lanes hold one block
 
@@ -156,7 +158,7 @@ def test_plan_headline_geometry(lib):
     assert b["grid"] == 2 * SM
     assert b["workspace_bytes"] == 2 * b["grid"] * 4096 * 4       # (high, low) rows per chunk
     q = rmsn.rmsn_plan(rmsn.OP_FUSED_QUANT, 8192, 4096, 1, 1)
-    assert (q["consumer_warps"], q["chunks_per_lane"], q["ctas_per_sm"], q["stages"]) == (8, 2, 3, 2)
+    assert (q["consumer_warps"], q["chunks_per_lane"], q["ctas_per_sm"], q["stages"]) == (8, 2, 3, 1)
 
 
 @pytest.mark.parametrize("H,xd,geom", [
