@@ -41,7 +41,7 @@ struct Policy {
 constexpr int kOps = 5;
 constexpr Policy kDefaultPolicy[kOps] = {
     {0, 4, 2, 4, 16},  // forward: small CTAs, 4 per SM, two stages each
-    {0, 0, 4, 2, 8},   // backward: 8 consumer warps at H >= 4096, 16 warps per SM
+    {0, 0, 4, 2, 8},   // backward: 8 consumer warps at bf16 H 4096-6144, 16 per SM in all
     {0, 3, 1, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM, one stage
     {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
     {0, 0, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
