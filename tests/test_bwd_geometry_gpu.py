@@ -1,5 +1,6 @@
-"""GPU parity of the strip backward in every launch geometry its plan picks (T above the
-small-T route, so the deterministic calls run the strip kernel and the column reduce):
+"""GPU parity of the strip backward in every class of launch geometry its plan picks (T
+above the small-T route, so the deterministic calls run the strip kernel and the column
+reduce):
 4 CTAs of 4 warps, 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
 2 CTAs of 8 warps with rows one at a time (bf16, about three vectors per lane) and one CTA
 of 16 warps (rows of at least 1024 vectors), each against the FP64 oracle, with plain and
@@ -29,6 +30,13 @@ GEOMETRIES = [
     (300, 16384, BF, F32, 16, 4, 1),
     (513, 4096, F32, F32, 16, 2, 1),
     (300, 8192, F32, BF, 16, 4, 1),
+    (700, 384, BF, F32, 1, 2, 16),
+    (500, 7168, BF, BF, 8, 4, 2),
+    (400, 9216, BF, F32, 16, 3, 1),   # rows in pairs, re-read from the stages
+    (400, 12288, BF, F32, 16, 3, 1),  # rows one at a time with 16 warps
+    (700, 384, F32, F32, 2, 2, 8),
+    (600, 2560, F32, BF, 8, 3, 2),
+    (600, 3584, F32, F32, 8, 4, 2),
 ]
 IDS = [f"T{g[0]}-H{g[1]}-{'bf16' if g[2] == BF else 'fp32'}" for g in GEOMETRIES]
 
