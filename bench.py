@@ -678,8 +678,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; x, dy ~ N(0,1), residual ~ N(0,2), w = 1 + 0.1 N(0,1))",
         "config": {"workload": WORKLOAD, "T": T_MAIN, "H": H_MAIN, "x_dtype": "bf16",
                    "w_dtype": "bf16", "accumulate": "fp32", "bwd_mode": "deterministic",
-                   "l2": "flushed before every timed op (512 MiB write + 256 MiB read, outside "
-                         "the events)",
+                   "l2": "flush (512 MiB write + 256 MiB read) ahead of each timed op, outside "
+                         "the events",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": {"bwd": "rmsnorm_bwd (main strip kernel + dW "

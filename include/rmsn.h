@@ -113,9 +113,9 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
 /* ------------------------------------------------------------------------------------
  * rmsnorm_bwd -- fused single-pass RMSNorm backward: dx and dw together.
  *
- * Sources: FlashInfer PR #5741, Design/Backward: a persistent grid over static row
- * chunks; each CTA writes dx for its rows, dx = rstd * (g*w - mean(g*w*xhat) * xhat) in
- * FP32, and keeps an FP32 dw partial for its chunk; the partials are then reduced per
+ * Sources: FlashInfer PR #5741, Design/Backward: persistent CTAs, each owning a fixed
+ * chunk of rows, compute dx = rstd * (dy*w - xhat * mean(dy*w*xhat)) for their rows in
+ * FP32 and hold one FP32 dw partial per chunk; the partials are then reduced per
  * column in chunk order, without atomics.  Liger-Kernel PR #1336, Summary: the fused
  * dX+dW strip-reduction backward.  miles-ext-kernels PR #15, Changes: the
  * deterministic ("det") and non-deterministic ("fast") backward, and TwoSum per-thread
@@ -219,9 +219,9 @@ int rmsnorm_fwd_residual(const void* x, const void* residual, int x_dtype, const
 /* ------------------------------------------------------------------------------------
  * rmsnorm_bwd_residual -- the backward of rmsnorm_fwd_residual.
  *
- * Source: FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward ("the residual variant
- * adds g_residual into the dx it returns (dx_total), so both inputs of the residual add
- * receive the same gradient tensor") and API (the backward takes h_new, w, rstd and
+ * Source: FlashInfer PR #5741 "cake_rmsnorm_train", Design/Backward (the residual backward
+ * returns dx + g_residual as dx_total, the one gradient that x and residual, the two
+ * addends of h_new, both receive) and API (the backward takes h_new, w, rstd and
  * g_residual).
  *
  *   dx_total[i, j] = round(rstd[i] * (dy*w - xhat * c_i)[j] + g_residual[i, j])  (FP32, one

@@ -13,8 +13,8 @@ benchmark's sampled self-check).  Tolerances:
 * dW (fp32): ``|dw - ref| <= 1e-4 + 1e-4*|ref|`` against the FP64 sum at the saved rstd
   (miles-ext-kernels PR #15, Accuracy: the weight-gradient budget).
 * fp8 codes and block scales: bit-exact, the oracle quantizing the device's own bf16
-  normed output (FlashInfer PR #4480, Summary: the fp8 is quantized from the
-  bf16-rounded normed so it matches normed_out).
+  normed output (FlashInfer PR #4480, Summary: the codes come from the normed values after
+  their rounding to bf16, the same values that normed_out holds).
 """
 from __future__ import annotations
 
