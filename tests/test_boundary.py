@@ -202,6 +202,26 @@ def test_set_policy(lib):
     assert (p["threads"], p["consumer_warps"]) == (160, 4)
 
 
+def test_set_policy_backward_sixteen_warps(lib):
+    # the backward ops take up to 16 consumer warps (one CTA per SM); the forward ops do not
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_FUSED_QUANT, consumer_warps=16)
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=32)
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=12)
+    for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
+        try:
+            rmsn.rmsn_set_policy(op, consumer_warps=16)
+            p = rmsn.rmsn_plan(op, 8192, 4096, 1, 1)
+            assert (p["consumer_warps"], p["ctas_per_sm"], p["threads"]) == (16, 1, 512)
+            assert p["chunks_per_lane"] == 1 and p["grid"] == SM
+        finally:
+            rmsn.rmsn_set_policy(op)
+        p = rmsn.rmsn_plan(op, 8192, 4096, 1, 1)
+        assert (p["consumer_warps"], p["ctas_per_sm"]) == (8, 2)
+
+
 def test_binding_rejects_cpu_tensors(lib):
     import torch
     x = torch.randn(4, 64)
