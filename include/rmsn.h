@@ -344,12 +344,19 @@ int rmsn_selftest_wait_timeout(uint64_t limit_ns, rmsn_stream_t stream);
  * Arguments, layouts and results are those of rmsnorm_bwd with deterministic = 1 (the
  * same kernels, so the same dx and, for the same device, dw).  The caller still provides
  * dy, x, w, rstd, dx and dw.
- *   - Returns RMSN_ERR_SCRATCH_LIMIT (nothing enqueued) when the call would need more than
- *     RMSN_NOALLOC_SCRATCH_BYTES of scratch, i.e. when 8 * H * (row chunks) exceeds it,
- *     the chunks being min(T, SMs * CTAs per SM) as rmsn_plan reports them (on a 152-SM
- *     GB300 with bf16 x: H <= 8192 always fits; H = 16384 fits up to T = 128).
+ *   - Calls with T <= rmsn_small_t_max() take the one-launch small-T route, which uses no
+ *     scratch, so every supported H is accepted there.  Longer calls take the strip route,
+ *     whose scratch is the workspace_bytes that rmsn_plan reports for RMSN_OP_BWD
+ *     (8 * H * row chunks, the chunks being min(T, SMs * CTAs per SM)); when that exceeds
+ *     RMSN_NOALLOC_SCRATCH_BYTES the call returns RMSN_ERR_SCRATCH_LIMIT and enqueues
+ *     nothing.  On a 152-SM GB300 at the default policy the strip route fits for fp32 x
+ *     at every supported H and for bf16 x at H <= 6896 and 8192 <= H <= 13792; the other
+ *     bf16 widths (e.g. 16384) are accepted up to the small-T threshold only.
  *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current, whichever route the call takes); make that first call
+ *     before any stream capture.  The address is kept for the life of the process, so
+ *     the library must not be used across cudaDeviceReset (the same holds for the
+ *     device error word of rmsn_device_status).
  *   - All calls in the process share the one array.  Every call writes all the scratch it
  *     reads, so nothing has to start at zero, but calls that overlap on the GPU (on
  *     different streams, or from several host threads without ordering) race on the

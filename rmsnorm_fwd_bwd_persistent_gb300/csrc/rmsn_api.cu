@@ -571,7 +571,8 @@ extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, int x_dtype, c
     int64_t need = 0;
     int st = plan_current(RMSN_OP_BWD, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
-    if (need > (int64_t)RMSN_NOALLOC_SCRATCH_BYTES) return RMSN_ERR_SCRATCH_LIMIT;
+    // The address lookup comes first on every route, so a device's first call always does
+    // it (the header asks for that first call to precede any stream capture).
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -579,9 +580,12 @@ extern "C" int rmsnorm_bwd_noalloc(const void* dy, const void* x, int x_dtype, c
     }
     void* scratch = noalloc_scratch(dev);
     if (!scratch) return RMSN_ERR_CUDA;
-    if (small_t(1, T))  // the one-launch small-T kernel needs no scratch
+    // The one-launch small-T kernel needs no scratch, so the limit applies to the strip route
+    // only.
+    if (small_t(1, T))
         return from_cuda(rmsn::launch_bwd_small(dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                                 compensated, s));
+    if (need > (int64_t)RMSN_NOALLOC_SCRATCH_BYTES) return RMSN_ERR_SCRATCH_LIMIT;
     return from_cuda(rmsn::launch_bwd(L, dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                       /*deterministic=*/1, compensated,
                                       static_cast<float*>(scratch), s));

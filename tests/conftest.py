@@ -24,3 +24,23 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Widening statistics of the bf16 dx gates (elements that needed the a-priori FP32
+    bound on top of one ulp, and their error in bf16 ulps of their row's RMS)."""
+    mod = sys.modules.get("_parity")
+    rec = getattr(mod, "WIDENING", None) if mod else None
+    if not rec:
+        return
+    n = sum(r["n"] for r in rec)
+    nw = sum(r["n_widened"] for r in rec)
+    worst = max(rec, key=lambda r: r["n_widened"] / max(r["n"], 1))
+    tr = terminalreporter
+    tr.section("bf16 dx gate widening")
+    tr.write_line(f"{len(rec)} bf16 dx comparisons, {n} elements: {nw} widened "
+                  f"({nw / max(n, 1):.2e}); max error of unwidened elements "
+                  f"{max(r['max_err_in_ulp'] for r in rec):.3f} ulp; max widened error "
+                  f"{max(r['max_widened_err_row_ulp'] for r in rec):.3e} row-RMS ulp")
+    tr.write_line(f"largest widened fraction: {worst['what']}: {worst['n_widened']} of "
+                  f"{worst['n']}")

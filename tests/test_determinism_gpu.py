@@ -47,3 +47,40 @@ def test_twosum_large_t(compensated):
     print(f"{c.name} compensated={compensated}: dw worst/budget = {r['dw']['worst']:.4f}, "
           f"rel_l2 = {r['dw']['rel_l2']:.3e}")
     P.assert_ok(r, c.name)
+
+
+# The non-deterministic ("fast") mode carries the same dW budget: its cross-chunk sum must
+# stay within atol 1e-4 + rtol 1e-4 of the FP64 sum at the sweep's largest T and at the
+# large-T compensated config (miles-ext-kernels PR #15, Accuracy: the budget applies to
+# every weight-gradient route, the non-deterministic package included).
+FAST_LARGE = [c for c in wl.DET_SWEEP if c.T == 131072] + [wl.TWOSUM_LARGE]
+
+
+@pytest.mark.parametrize("c", FAST_LARGE, ids=[c.name for c in FAST_LARGE])
+@pytest.mark.parametrize("compensated", [False, True])
+def test_fast_mode_budget_at_large_t(c, compensated):
+    x, dy, w = wl.fwd_bwd_inputs(c, DEV, seed=0)
+    _, rstd = rmsn.rmsnorm_fwd(x, w, c.eps)
+    r = P.check_bwd(dy, x, w, rstd, deterministic=False, compensated=compensated)
+    print(f"{c.name} fast compensated={compensated}: dw worst/budget = {r['dw']['worst']:.4f}")
+    P.assert_ok(r, f"{c.name} fast")
+
+
+# Every row of dx compared with the oracle (in chunks), not a sample: the long strips of the
+# deterministic backward at T = 65536 (216 rows per CTA), the sweep's largest row count at
+# its widest rows, and the large-T compensated config.
+FULL_ROWS = [wl.Workload("det_bwd_t65536_h4096_bf16w", 65536, 4096, torch.bfloat16,
+                         torch.bfloat16),
+             next(c for c in wl.DET_SWEEP if c.T == 131072 and c.H == 6144),
+             wl.TWOSUM_LARGE]
+
+
+@pytest.mark.parametrize("c", FULL_ROWS, ids=[c.name for c in FULL_ROWS])
+def test_every_row_at_large_t(c):
+    x, dy, w = wl.fwd_bwd_inputs(c, DEV, seed=3)
+    r = P.check_fwd(x, w, c.eps, all_rows=True)
+    P.assert_ok(r, f"{c.name} fwd")
+    rb = P.check_bwd(dy, x, w, r["_rstd_dev"], deterministic=True,
+                     compensated=c is wl.TWOSUM_LARGE, all_rows=True)
+    assert rb["dx"]["n"] == c.T * c.H
+    P.assert_ok(rb, f"{c.name} bwd")

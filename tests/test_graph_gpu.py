@@ -1,10 +1,13 @@
-"""The three operations captured in one CUDA graph and replayed give the bits of eager calls
-(the entry points enqueue only kernels, a memset-free launch sequence and the programmatic
+"""The three operations captured in one CUDA graph and replayed: every replay matches the
+FP64 oracle under the same gates as the eager parity tests (fresh inputs written into the
+captured buffers between replays), and gives the bits of eager calls on the same data (the
+entry points enqueue only kernels, a memset-free launch sequence and the programmatic
 dependent launch of the dW reduce, all capturable).  Every set-up the library does once
 (device properties, kernel attributes, occupancy) happens in the eager calls first."""
 import pytest
 import torch
 
+import _parity as P
 import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
 import workloads as wl
 
@@ -46,8 +49,16 @@ def test_graph_replay_matches_eager(T):
         eager = outputs()
         run(eager)
         g_out["res"].copy_(fres0)  # the fused op updates residual in place
+        res_in = wl.to_oracle(fres0).copy()
         graph.replay()
         torch.cuda.synchronize()
+        # the replay against the oracle
+        o = g_out
+        P.assert_ok(P.gate_fwd(x, w, c.eps, o["y"], o["rstd"]), f"graph fwd rep {rep}")
+        P.assert_ok(P.gate_bwd(dy, x, w, o["rstd"], o["dx"], o["dw"], True), f"graph bwd rep {rep}")
+        P.assert_ok(P.gate_fused(fx, res_in, fw, c.eps, o["q"], o["sc"], o["nm"], o["res"]),
+                    f"graph fused rep {rep}")
+        # and bit for bit against eager calls on the same data
         for k in eager:
             a, b = eager[k], g_out[k]
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (rep, k)

@@ -153,6 +153,13 @@ def test_fused_config():
     P.assert_ok(P.check_fused(x, res, w, c.eps), c.name)
 
 
+def test_fused_bench_shape():
+    """The fused op at the shape the benchmark's step times (T = 8192, H = 4096)."""
+    c = wl.FUSED_QUANT_MAIN
+    x, res, w = wl.fused_inputs(c, DEV, seed=4)
+    P.assert_ok(P.check_fused(x, res, w, c.eps), c.name)
+
+
 def test_fused_zero_and_special_blocks():
     T, H = 12, 1024
     x, res, w = wl.fused_inputs(_wl(wl.FUSED_QUANT, T, H), DEV, seed=3)
