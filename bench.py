@@ -603,6 +603,60 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ------------------------------------------------------------------------- one op alone
+ONLY_OPS = ("fwd", "bwd", "bwd_fast", "fused_quant", "fwd_residual", "bwd_residual")
+
+
+def run_only(args):
+    """One op at T x H bf16 (inputs seeded as in the step), --warmup + --launches calls,
+    nothing else allocated: what a profiler captures when it needs one kernel at a time."""
+    import dataclasses
+    import rmsnorm_fwd_bwd_persistent_gb300 as rmsn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, H, op = args.T, args.H, args.only
+    if op == "fused_quant":
+        c = dataclasses.replace(wl.FUSED_QUANT_MAIN, T=T, H=H)
+        x, res, w = wl.fused_inputs(c, dev, 1)
+        q = torch.empty(T, H, device=dev, dtype=torch.uint8)
+        sc = torch.empty(H // 128, wl.round_up(T, 4), device=dev)
+        nm = torch.empty_like(x)
+        fn = lambda: rmsn.fused_add_rmsnorm_fp8_block_quant(x, res, w, c.eps, q, sc, nm)  # noqa
+    elif op in ("fwd_residual", "bwd_residual"):
+        c = dataclasses.replace(wl.RESIDUAL_MAIN, T=T, H=H)
+        x, res, dy, g, w = wl.residual_inputs(c, dev, 2)
+        y, h = torch.empty_like(x), torch.empty_like(x)
+        rstd = torch.empty(T, device=dev)
+        rmsn.rmsnorm_fwd_residual(x, res, w, c.eps, y=y, h_new=h, rstd=rstd)
+        if op == "fwd_residual":
+            fn = lambda: rmsn.rmsnorm_fwd_residual(x, res, w, c.eps, y=y, h_new=h, rstd=rstd)  # noqa
+        else:
+            dxt, dw = torch.empty_like(x), torch.empty(H, device=dev)
+            ws = torch.empty(rmsn.rmsnorm_bwd_workspace_bytes(T, H, False, dev), device=dev,
+                             dtype=torch.uint8)
+            fn = lambda: rmsn.rmsnorm_bwd_residual(dy, h, w, rstd, g, True, False, ws, dxt, dw)  # noqa
+    else:
+        c = dataclasses.replace(wl.MAIN_BF16, T=T, H=H)
+        x, dy, w = wl.fwd_bwd_inputs(c, dev, 0)
+        y, rstd = torch.empty_like(x), torch.empty(T, device=dev)
+        rmsn.rmsnorm_fwd(x, w, c.eps, y=y, rstd=rstd)
+        if op == "fwd":
+            fn = lambda: rmsn.rmsnorm_fwd(x, w, c.eps, y=y, rstd=rstd)  # noqa
+        else:
+            det = op == "bwd"
+            dx, dw = torch.empty_like(x), torch.empty(H, device=dev)
+            ws = torch.empty(max(rmsn.rmsnorm_bwd_workspace_bytes(T, H, False, dev), 16),
+                             device=dev, dtype=torch.uint8)
+            fn = lambda: rmsn.rmsnorm_bwd(dy, x, w, rstd, det, False, ws, dx, dw)  # noqa
+    for _ in range(args.warmup + args.launches):
+        fn()
+    torch.cuda.synchronize()
+    st = rmsn.rmsn_device_status()
+    print(json.dumps({"only": op, "T": T, "H": H, "calls": args.warmup + args.launches,
+                      "device_status": st}), flush=True)
+    return 0 if st == 0 else 1
+
+
 # ------------------------------------------------------------------------------ main
 def main(argv=None):
     ap = argparse.ArgumentParser()
@@ -612,7 +666,16 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=sorted(ONLY_OPS),
+                    help="run one op alone at --T x --H (bf16) for --launches calls after "
+                         "--warmup calls, allocating only its own buffers (a small process "
+                         "for a profiler to capture); prints one line, times nothing")
+    ap.add_argument("--T", type=int, default=T_MAIN)
+    ap.add_argument("--H", type=int, default=H_MAIN)
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.only:
+        return run_only(args)
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = _dist_env()
@@ -664,6 +727,8 @@ def run_ours(args, world, rank, local):
         gbs = step.bytes[op] / (op_ms[op] * 1e-3) / 1e9
         ops[op] = {"us_median": us, "us_mean": op_ms[op] * 1e3, "gbs": gbs, "frac": gbs / peak,
                    "bytes": step.bytes[op], "launches": Step.LAUNCHES[op]}
+    per_op = {op: {"us_mean": ops[op]["us_mean"], "gbs": ops[op]["gbs"], "frac": ops[op]["frac"],
+                   "bytes": ops[op]["bytes"]} for op in Step.OPS}
     dom = max(Step.OPS, key=lambda o: op_ms[o])
     achieved = step.bytes[dom] / (op_ms[dom] * 1e-3) / 1e9
     traffic = recorded_traffic(dom)
@@ -688,7 +753,7 @@ def run_ours(args, world, rank, local):
                                                 "fused_quant": "fused_add_rmsnorm_fp8_kernel"}[dom],
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": step.bytes[dom],
-                     "peak_source": peak_src},
+                     "peak_source": peak_src, "per_op": per_op},
         "ops_residual_variant": {k: dict(v, frac=v["gbs"] / peak) for k, v in extra.items()},
         "bwd_small_t_route": small,
         "bwd_long_strip": long_strip,

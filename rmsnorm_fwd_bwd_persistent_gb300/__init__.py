@@ -196,13 +196,11 @@ def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.
     _cuda(dw, "dw")
     if dx.shape != x.shape or dx.dtype != x.dtype or dw.shape != (H,) or dw.dtype != torch.float32:
         raise ValueError("dx must match x; dw must be float32 [H]")
-    ws_ptr, ws_bytes = None, 0
-    if deterministic:
-        if workspace is None:
-            n = rmsnorm_bwd_workspace_bytes(T, H, compensated, x.device)
-            workspace = torch.empty(max(n, 16), device=x.device, dtype=torch.uint8)
-        _cuda(workspace, "workspace")
-        ws_ptr, ws_bytes = _p(workspace), workspace.numel() * workspace.element_size()
+    if workspace is None:
+        n = rmsnorm_bwd_workspace_bytes(T, H, compensated, x.device)
+        workspace = torch.empty(max(n, 16), device=x.device, dtype=torch.uint8)
+    _cuda(workspace, "workspace")
+    ws_ptr, ws_bytes = _p(workspace), workspace.numel() * workspace.element_size()
     with torch.cuda.device(x.device):
         st = load_library().rmsnorm_bwd(_p(dy), _p(x), _dt(x), _p(w), _dt(w), _p(rstd), _p(dx),
                                         _p(dw), T, H, int(bool(deterministic)),
@@ -260,13 +258,11 @@ def rmsnorm_bwd_residual(dy: torch.Tensor, h: torch.Tensor, w: torch.Tensor, rst
     if dx_total.shape != h.shape or dx_total.dtype != h.dtype or dw.shape != (H,) or \
             dw.dtype != torch.float32:
         raise ValueError("dx_total must match h; dw must be float32 [H]")
-    ws_ptr, ws_bytes = None, 0
-    if deterministic:
-        if workspace is None:
-            n = rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
-            workspace = torch.empty(max(n, 16), device=h.device, dtype=torch.uint8)
-        _cuda(workspace, "workspace")
-        ws_ptr, ws_bytes = _p(workspace), workspace.numel() * workspace.element_size()
+    if workspace is None:
+        n = rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
+        workspace = torch.empty(max(n, 16), device=h.device, dtype=torch.uint8)
+    _cuda(workspace, "workspace")
+    ws_ptr, ws_bytes = _p(workspace), workspace.numel() * workspace.element_size()
     with torch.cuda.device(h.device):
         st = load_library().rmsnorm_bwd_residual(
             _p(dy), _p(h), _dt(h), _p(w), _dt(w), _p(rstd), _p(g_residual), _p(dx_total), _p(dw),

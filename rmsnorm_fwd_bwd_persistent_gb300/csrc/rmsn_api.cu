@@ -200,7 +200,9 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     L->smem = data_off + stages * stage_bytes;
     L->err = nullptr;
     L->limit_ns = kWaitLimitNs;
-    if (ws_bytes) *ws_bytes = is_bwd ? grid * H * 4 * 2 : 0;
+    // the backward's workspace: the chunk partials (deterministic mode) or the two column
+    // sums and the ticket counter of the atomic mode, whichever is larger
+    if (ws_bytes) *ws_bytes = is_bwd ? std::max<int64_t>(grid * H * 4 * 2, H * 4 * 2 + 256) : 0;
     return RMSN_OK;
 }
 
@@ -276,8 +278,12 @@ cudaError_t fit_grid(const void* kernel, const Launch& L, int threads, int64_t* 
         for (const auto& x : opted)
             if (x.dev == dev && x.k == kernel) done = true;
         if (!done) {
+            // the opt-in maximum covers static and dynamic shared memory together
+            cudaFuncAttributes fa{};
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)p->smem_cta);
+                                     (int)(p->smem_cta - (int64_t)fa.sharedSizeBytes));
             if (e != cudaSuccess) return e;
             opted.push_back({dev, kernel});
         }
@@ -443,14 +449,13 @@ int rmsnorm_bwd(const void* dy, const void* x, int x_dtype, const void* w, int w
     if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(w, 16) || !aligned(dx, 16) ||
         !aligned(rstd, 4))
         return RMSN_ERR_MISALIGNED;
-    if (deterministic && !workspace)
-        return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
-    if (deterministic && !aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
+    if (!workspace) return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
     Launch L{};
     int64_t need = 0;
     int st = plan_current(RMSN_OP_BWD, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
-    if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if ((int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
     if (small_t(deterministic, T))
         return from_cuda(rmsn::launch_bwd_small(dy, x, x_dtype, w, w_dtype, rstd, dx, dw, T, H,
                                                 compensated, s));
@@ -491,14 +496,13 @@ int rmsnorm_bwd_residual(const void* dy, const void* h, int x_dtype, const void*
     if (!aligned(dy, 16) || !aligned(h, 16) || !aligned(w, 16) || !aligned(g_residual, 16) ||
         !aligned(dx_total, 16) || !aligned(rstd, 4))
         return RMSN_ERR_MISALIGNED;
-    if (deterministic && !workspace)
-        return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
-    if (deterministic && !aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
+    if (!workspace) return workspace_bytes ? RMSN_ERR_INVALID_ARG : RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return RMSN_ERR_MISALIGNED;
     Launch L{};
     int64_t need = 0;
     int st = plan_current(RMSN_OP_BWD_RESIDUAL, T, H, x_dtype, w_dtype, &L, &need);
     if (st != RMSN_OK) return st;
-    if (deterministic && (int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
+    if ((int64_t)workspace_bytes < need) return RMSN_ERR_WORKSPACE_TOO_SMALL;
     if (small_t(deterministic, T))
         return from_cuda(rmsn::launch_bwd_small(dy, h, x_dtype, w, w_dtype, rstd, dx_total, dw, T,
                                                 H, compensated, s, g_residual));

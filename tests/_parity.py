@@ -176,7 +176,7 @@ def check_bwd(dy, x, w, rstd, deterministic=True, compensated=False, full_dw=Tru
     T, H = x.shape
     dxbuf, dx = guarded((T, H), x.dtype, x.device)
     dwbuf, dw = guarded((H,), torch.float32, x.device)
-    if deterministic and workspace is None:
+    if workspace is None:  # NaN-poisoned: no call may depend on what it held before
         n = rmsn.rmsnorm_bwd_workspace_bytes(T, H, compensated, x.device)
         workspace = torch.full((max(n, 16) // 4,), float("nan"), device=x.device,
                                dtype=torch.float32)
@@ -234,10 +234,8 @@ def check_bwd_residual(dy, h, w, rstd, g_res, deterministic=True, compensated=Fa
         dxbuf, dxt = None, dy
     else:
         dxbuf, dxt = guarded((T, H), h.dtype, h.device)
-    ws = None
-    if deterministic:
-        n = rmsn.rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
-        ws = torch.full((max(n, 16) // 4,), float("nan"), device=h.device, dtype=torch.float32)
+    n = rmsn.rmsnorm_bwd_workspace_bytes(T, H, compensated, h.device)
+    ws = torch.full((max(n, 16) // 4,), float("nan"), device=h.device, dtype=torch.float32)
     rmsn.rmsnorm_bwd_residual(dy, h, w, rstd, g_res, deterministic=deterministic,
                               compensated=compensated, workspace=ws, dx_total=dxt, dw=dw)
     torch.cuda.synchronize()

@@ -74,6 +74,10 @@ def test_bwd_argument_checks(lib):
     assert b(A, A, 3, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID
     assert b(None, A, 1, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == INVALID
     assert b(A, A + 2, 1, A, 0, A, A, A, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
+    # both modes need the workspace (the atomic mode keeps its column sums there)
+    assert b(A, A, 1, A, 0, A, A, A, 4, 64, 1, 0, None, 0, None) == WS_SMALL
+    assert b(A, A, 1, A, 0, A, A, A, 4, 64, 0, 0, None, 0, None) == WS_SMALL
+    assert b(A, A, 1, A, 0, A, A, A, 4, 64, 0, 0, A + 8, 1 << 20, None) == MISALIGNED
 
 
 def test_fused_argument_checks(lib):
@@ -104,6 +108,7 @@ def test_residual_argument_checks(lib):
     assert b(A, A, 1, A, 0, A, A + 8, A, A, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
     assert b(A, A, 1, A, 0, A, A, A, A + 4, 4, 64, 1, 0, A, 1 << 20, None) == MISALIGNED
     assert b(A, A, 1, A, 0, A, A, A, A, 4, 64, 1, 0, None, 0, None) == WS_SMALL
+    assert b(A, A, 1, A, 0, A, A, A, A, 4, 64, 0, 0, None, 0, None) == WS_SMALL  # atomic mode too
 
 
 SM = 152
