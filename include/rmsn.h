@@ -101,8 +101,7 @@ int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y,
  *
  * The workspace holds, per row chunk, the chunk's dw partial as two FP32 rows (the
  * high and low parts of a compensated sum): 8 * H bytes per chunk, at most
- * (SM count x CTAs per SM) chunks and never more than T; at least 8 * H + 256 bytes (the
- * two FP32 column sums and the ticket counter of deterministic = 0).  The value returned for (T, H)
+ * (SM count x CTAs per SM) chunks and never more than T.  The value returned for (T, H)
  * is an upper bound for every T' <= T with the same H and device, so one buffer can be
  * reused across calls.  `device` is a CUDA device ordinal (its SM count decides the
  * number of chunks); `compensated` does not change the size.  The same bound serves
@@ -134,14 +133,10 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *         library build and the launch policy) only.  For T <= rmsn_small_t_max() (256
  *         by default) one kernel does the whole backward instead, with dw summed over
  *         all rows per column slab in a fixed order (see rmsn_set_small_t_max).
- *         == 0: the chunk partials are combined with atomics instead (no second kernel):
- *         each chunk adds its high part to an FP32 column sum in the workspace with
- *         atomicAdd, takes that addition's exact rounding error from the value the atomic
- *         returns (TwoSum) and adds it, with its low part, to a second column sum; the
- *         last chunk to finish writes dw = high sum + low sum.  The accuracy matches the
- *         deterministic mode at every T (the same weight-gradient budget); the bits may
- *         differ from run to run (the order of the additions depends on scheduling).  One
- *         memset of 8 * H + 16 bytes of the workspace precedes the kernel.
+ *         == 0: allows the library any order of the cross-chunk sum.  On GB300 the
+ *         fixed-order reduction above is faster than the atomic sums measured (and plain
+ *         FP32 atomics leave the weight-gradient budget at large T), so this setting runs
+ *         the same kernels and its bits are reproducible too.
  *   compensated  != 0: each thread adds every product dy*xhat to an FP32 (high, low)
  *         pair with the error-free TwoSum transformation.
  *         == 0: each thread sums the products of the two rows of each row pair it
@@ -155,7 +150,7 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t H, int compensated, int de
  *   workspace, workspace_bytes  device scratch of at least
  *         rmsnorm_bwd_workspace_bytes(T, H, compensated, device) bytes, 16-byte
  *         aligned; its contents on entry do not matter and on exit are unspecified.
- *         Needed in both modes.
+ *         Needed with either setting of deterministic.
  *   x_dtype fp32 supports H <= 8192 (bf16: H <= RMSN_MAX_H).
  * Returns RMSN_OK or an error status (see conventions).
  * ---------------------------------------------------------------------------------- */

@@ -200,9 +200,8 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     L->smem = data_off + stages * stage_bytes;
     L->err = nullptr;
     L->limit_ns = kWaitLimitNs;
-    // the backward's workspace: the chunk partials (deterministic mode) or the two column
-    // sums and the ticket counter of the atomic mode, whichever is larger
-    if (ws_bytes) *ws_bytes = is_bwd ? std::max<int64_t>(grid * H * 4 * 2, H * 4 * 2 + 256) : 0;
+    // the backward's workspace: the chunks' (high, low) partial rows
+    if (ws_bytes) *ws_bytes = is_bwd ? grid * H * 4 * 2 : 0;
     return RMSN_OK;
 }
 

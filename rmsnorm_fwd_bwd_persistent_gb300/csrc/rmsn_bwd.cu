@@ -29,12 +29,10 @@
 // prefetches each row's g_residual into L2 (bulk prefetch) when it issues the row's copies,
 // and pass 2 reads it from global memory and adds it to the FP32 dx before the one
 // rounding to x's dtype.
-// At the end of the strip the CTA writes its (high, low) partial row to the workspace
-// (deterministic mode), or (atomic mode) adds its high part to a zeroed FP32 column sum with
-// atomicAdd, recovers that addition's exact rounding error from the value the atomic returns
-// (TwoSum), and adds the error plus its low part to a second column sum; the last CTA to
-// finish (a ticket counter) writes dw = high sum + low sum.  The cross-chunk sum is then as
-// accurate as the deterministic one, in an order that depends on scheduling.
+// At the end of the strip the CTA writes its (high, low) partial row to the workspace.
+// Both settings of `deterministic` take this fixed-order path: on GB300 it is faster than
+// the atomic cross-chunk sums tried (plain FP32 atomics also leave the weight-gradient
+// budget at large T).
 //
 // Column reduce kernel: dw[j] = sum over chunks of the (high, low) partials, in a fixed
 // order (contiguous chunk ranges summed in chunk order, then a fixed binary tree over the
@@ -55,9 +53,8 @@ struct BwdArgs {
     const void* w;
     const float* rstd;
     void* dx;
-    float* dw;   // written by the reduce (deterministic) or by the last CTA (atomic mode)
-    float* ws;   // deterministic mode: [n_chunks, H] high parts, then [n_chunks, H] low parts;
-                 // atomic mode: zeroed [H] high sums, [H] low sums, then a CTA counter
+    float* dw;   // written by the column reduce
+    float* ws;   // [n_chunks, H] high parts, then [n_chunks, H] low parts
     const void* gres;  // residual variant: g_residual rows (x's dtype)
     unsigned* err;
     int64_t T;
@@ -69,7 +66,6 @@ struct BwdArgs {
     uint32_t stage_bytes;
     uint32_t w_bytes;
     uint32_t data_off;
-    int atomic;
 };
 
 template <typename TX, typename TW, int NCH, bool COMP, bool RES, bool SINGLE>
@@ -333,48 +329,15 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
         const int v = c * NC + t;
         if (v < nvec) {
             const int col0 = v * VEC;
-            if (a.atomic) {
-                float* sum_hi = a.ws;
-                float* sum_lo = a.ws + H;
+            f2* dh = reinterpret_cast<f2*>(a.ws + (int64_t)blockIdx.x * H + col0);
+            f2* dl = reinterpret_cast<f2*>(a.ws + (nch + (int64_t)blockIdx.x) * H + col0);
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = col0 + 2 * i + e;
-                        const float h = e ? f2_hi(hi[c][i]) : f2_lo(hi[c][i]);
-                        const float l = e ? f2_hi(lo[c][i]) : f2_lo(lo[c][i]);
-                        const float old = atomicAdd(sum_hi + j, h);
-                        float sum, err;
-                        two_sum(old, h, sum, err);  // old + h == sum + err exactly
-                        atomicAdd(sum_lo + j, __fadd_rn(l, err));
-                    }
-                }
-            } else {
-                f2* dh = reinterpret_cast<f2*>(a.ws + (int64_t)blockIdx.x * H + col0);
-                f2* dl = reinterpret_cast<f2*>(a.ws + (nch + (int64_t)blockIdx.x) * H + col0);
-#pragma unroll
-                for (int i = 0; i < NP; i += 2) {
-                    *reinterpret_cast<ulonglong2*>(dh + i) = make_ulonglong2(hi[c][i], hi[c][i + 1]);
-                    *reinterpret_cast<ulonglong2*>(dl + i) = make_ulonglong2(lo[c][i], lo[c][i + 1]);
-                }
+            for (int i = 0; i < NP; i += 2) {
+                *reinterpret_cast<ulonglong2*>(dh + i) = make_ulonglong2(hi[c][i], hi[c][i + 1]);
+                *reinterpret_cast<ulonglong2*>(dl + i) = make_ulonglong2(lo[c][i], lo[c][i + 1]);
             }
         }
     }
-    if (!a.atomic) return;
-
-    // ---- atomic mode: the last CTA to finish writes dw = high sum + low sum
-    __threadfence();  // this thread's atomics are performed before the ticket below
-    __syncthreads();
-    int* s_last = ring_flag(smem);  // in the ring header: the kernel has no static shared memory
-    if (threadIdx.x == 0) {
-        unsigned* tickets = reinterpret_cast<unsigned*>(a.ws + 2 * (int64_t)H);
-        *s_last = atomicAdd(tickets, 1u) == (unsigned)(nch - 1);
-        __threadfence();
-    }
-    __syncthreads();
-    if (!*s_last) return;
-    for (int j = t; j < H; j += blockDim.x)
-        a.dw[j] = __fadd_rn(__ldcg(a.ws + j), __ldcg(a.ws + H + j));
 }
 
 // dw[j] = fixed-order compensated sum over the chunk partials.  A CTA covers 16 columns
@@ -481,13 +444,9 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
                        int w_dt, const float* rstd, void* dx, float* dw, int64_t T, int64_t H,
                        int deterministic, int compensated, float* ws, cudaStream_t s,
                        const void* g_residual) {
+    (void)deterministic;  // both settings take the fixed-order reduction
     BwdArgs a{dy, x, w, rstd, dx, dw, ws, g_residual, L.err, T, L.limit_ns, (int)H, L.nw,
-              L.stages, L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off,
-              deterministic ? 0 : 1};
-    if (!deterministic) {  // the column sums and the ticket counter start at zero
-        cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)H * 2 * sizeof(float) + 16, s);
-        if (e != cudaSuccess) return e;
-    }
+              L.stages, L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off};
     cudaError_t e;
     int64_t g = 0;  // chunks the main kernel ran with
     if (x_dt == 1 && w_dt == 1) e = dispatch_comp<__nv_bfloat16, __nv_bfloat16>(L, a, compensated, s, &g);
@@ -495,7 +454,7 @@ cudaError_t launch_bwd(const Launch& L, const void* dy, const void* x, int x_dt,
     else if (x_dt == 0 && w_dt == 0) e = dispatch_comp<float, float>(L, a, compensated, s, &g);
     else if (x_dt == 0 && w_dt == 1) e = dispatch_comp<float, __nv_bfloat16>(L, a, compensated, s, &g);
     else return cudaErrorInvalidValue;
-    if (e != cudaSuccess || !deterministic) return e;
+    if (e != cudaSuccess) return e;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((H + 15) / 16));

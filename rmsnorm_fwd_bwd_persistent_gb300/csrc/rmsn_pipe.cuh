@@ -177,7 +177,6 @@ struct Slot {
 //   [512, 768)    red[2][32]    per-warp partial sums (one value per row)
 //   [768, 832)    abort[2][32]  per-warp "gave up" flags, one byte each
 //   [1024, 1536)  red2[2][32]   per-warp partial sums (two values, two rows at a time)
-//   [1536, 1540)  flag          one CTA-wide word (the backward's last-CTA decision)
 constexpr int kRingHeader = 2048;  // bytes reserved before the weights (S <= 32)
 
 __device__ __forceinline__ Ring ring_at(uint8_t* smem, int stages, uint32_t stage_bytes,
@@ -199,9 +198,6 @@ __device__ __forceinline__ uint8_t* ring_abort(uint8_t* smem) {
 }
 __device__ __forceinline__ float2* ring_red2(uint8_t* smem) {
     return reinterpret_cast<float2*>(smem + 1024);  // [2][32] per-warp partial sum pairs
-}
-__device__ __forceinline__ int* ring_flag(uint8_t* smem) {
-    return reinterpret_cast<int*>(smem + 1536);     // one CTA-wide word
 }
 
 // Initializes the barriers (thread 0) and makes them visible to the CTA.
