@@ -31,16 +31,23 @@ constexpr int kWarpsPerSm = 16;  // the backward's consumer warps per SM (measur
 // ------------------------------------------------------------------ policy defaults
 struct Policy {
     int consumer_warps;  // 0: derived from H (target_nch vectors per lane)
-    int ctas_per_sm;     // 0: kWarpsPerSm / consumer warps (backward)
-    int max_stages;
+    int ctas_per_sm;     // 0: derived (backward: kWarpsPerSm / consumer warps; forward: from
+                         // the row size, about kFwdBytesInFlight of rows per SM)
+    int max_stages;      // 0: derived (forward: two stages for rows of at most 4 KiB, else one)
     int target_nch;
     int max_nch;
 };
 
+// The forward's rows in flight per SM (ring stages of all its CTAs) for rows above 4 KiB:
+// a launch-policy sweep on GB300 (bf16 and fp32, H 1024-8192, T 8192 and 65536) found the
+// best CTAs per SM at about this many bytes of rows in flight, with one stage per CTA.
+constexpr int64_t kFwdBytesInFlight = 48 << 10;
+
 // Per op: FWD, BWD, FUSED, FWD_RESIDUAL, BWD_RESIDUAL.
 constexpr int kOps = 5;
 constexpr Policy kDefaultPolicy[kOps] = {
-    {0, 4, 2, 4, 16},  // forward: small CTAs, 4 per SM, two stages each
+    {0, 0, 0, 6, 16},  // forward: at least 2 warps, about 6 vectors per lane, CTAs and
+                       // stages from the row size
     {0, 0, 4, 2, 8},   // backward: 8 consumer warps at bf16 H 4096-6144, 16 per SM in all
     {0, 3, 1, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM, one stage
     {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
@@ -145,11 +152,18 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     const int64_t nvec = H / vec;
     int nw = P.consumer_warps;
     if (nw == 0) {
-        nw = 1;
+        nw = op == RMSN_OP_FWD ? 2 : 1;
         while (nw < 8 && cdiv(nvec, 32 * nw) > P.target_nch) nw *= 2;
         // backward rows that fill 16 warps at target_nch vectors per lane take 16 warps
         // (one CTA per SM), so every lane keeps its share of a row pair in registers
         if (is_bwd && nvec >= 16 * 32 * P.target_nch) nw = 16;
+        // bf16 rows of about three vectors per lane at 8 warps (H 5632-6144) over a short
+        // strip: one CTA of 16 warps per SM is faster up to T ~ 12288 (measured on GB300:
+        // 14-16% at T = 2048, 8-9% at 4096, 2-4% at 8192, even at 16384, slower above), its
+        // column reduce sums half as many chunks
+        if (is_bwd && x_dt == RMSN_BF16 && nw == 8 && T <= 12288 &&
+            cdiv(nvec, 32 * nw) == 3 && 4 * nvec >= 11 * 32 * (int64_t)nw)
+            nw = 16;
     }
     const int64_t need = cdiv(nvec, 32 * nw);
     int nch = 0;
@@ -166,8 +180,18 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     const int64_t stage_bytes = rows * row_pad;
     const int64_t w_bytes = H * 4;  // w is staged in shared memory as FP32
     const int64_t data_off = rmsn::kRingHeader + cdiv(w_bytes, 128) * 128;
-    // CTAs per SM: the policy's, or enough CTAs for kWarpsPerSm consumer warps per SM
-    int cps = P.ctas_per_sm > 0 ? P.ctas_per_sm : (nw >= kWarpsPerSm ? 1 : kWarpsPerSm / nw);
+    // CTAs per SM: the policy's; or enough CTAs for kWarpsPerSm consumer warps per SM
+    // (backward); or, for the forward, 8 for rows of at most 4 KiB and else about
+    // kFwdBytesInFlight / row size (one stage each), fewer if shared memory or registers
+    // run out (the grid is clamped to the resident CTAs at launch)
+    const bool small_rows = row_bytes <= 4096;
+    int cps = P.ctas_per_sm;
+    if (cps == 0 && op == RMSN_OP_FWD)
+        cps = small_rows ? 8
+                         : (int)std::max<int64_t>(2, std::min<int64_t>(
+                               8, (kFwdBytesInFlight + row_bytes / 2) / row_bytes));
+    if (cps == 0) cps = nw >= kWarpsPerSm ? 1 : kWarpsPerSm / nw;
+    const int max_stages = P.max_stages > 0 ? P.max_stages : (small_rows ? 2 : 1);
     auto stages_for = [&](int c) -> int64_t {
         int64_t share = smem_sm / c - kSmemReservedPerCta;
         if (share > smem_cta) share = smem_cta;
@@ -175,10 +199,13 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     };
     // the backward holds two rows' stages at once (it takes rows two at a time)
     const int64_t min_stages = is_bwd ? 2 : 1;
-    while (cps > 1 && stages_for(cps) < 2) --cps;
+    // room for two stages per CTA (the forward: for as many as it will use)
+    const int64_t want_stages =
+        op == RMSN_OP_FWD ? std::max<int64_t>(1, std::min<int64_t>(2, max_stages)) : 2;
+    while (cps > 1 && stages_for(cps) < want_stages) --cps;
     int64_t stages = stages_for(cps);
     if (stages < min_stages) return RMSN_ERR_UNSUPPORTED_SHAPE;
-    if (stages > P.max_stages) stages = P.max_stages > min_stages ? P.max_stages : min_stages;
+    if (stages > max_stages) stages = max_stages > min_stages ? max_stages : min_stages;
 
     int64_t grid = (int64_t)sms * cps;
     if (grid > T) grid = T;

@@ -147,8 +147,10 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         wpad = -(-(H * 4) // 128) * 128                           # w staged as FP32 in smem
         assert p["stages"] >= 1 and p["smem_bytes"] == 2048 + wpad + p["stages"] * stage
         assert p["ctas_per_sm"] * (p["smem_bytes"] + 1024) <= 233472  # fits the SM
-        if is_bwd or (p["ctas_per_sm"] > 1 and op != rmsn.OP_FUSED_QUANT):
+        if is_bwd or (p["ctas_per_sm"] > 1 and op == rmsn.OP_FWD_RESIDUAL):
             assert p["stages"] >= 2                                 # bwd holds two rows
+        if op == rmsn.OP_FWD:                                       # one stage above 4 KiB rows
+            assert p["stages"] == (2 if row <= 4096 else 1)
         if op == rmsn.OP_FUSED_QUANT:
             assert p["stages"] == 1                                 # one stage, 3 CTAs per SM
         if op == rmsn.OP_FUSED_QUANT:
@@ -157,7 +159,7 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
 
 def test_plan_headline_geometry(lib):
     f = rmsn.rmsn_plan(rmsn.OP_FWD, 8192, 4096, 1, 1)
-    assert (f["consumer_warps"], f["chunks_per_lane"], f["ctas_per_sm"], f["stages"]) == (4, 4, 4, 2)
+    assert (f["consumer_warps"], f["chunks_per_lane"], f["ctas_per_sm"], f["stages"]) == (4, 4, 6, 1)
     b = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1)
     assert (b["consumer_warps"], b["chunks_per_lane"], b["ctas_per_sm"]) == (8, 2, 2)
     assert b["grid"] == 2 * SM
@@ -179,6 +181,30 @@ def test_plan_backward_geometry_by_row_length(lib, H, xd, geom):
         assert p["consumer_warps"] * p["ctas_per_sm"] == 16
         assert p["grid"] == SM * p["ctas_per_sm"]
         assert p["workspace_bytes"] == 8 * H * p["grid"]
+
+
+def test_plan_backward_short_strip_rule(lib):
+    # bf16 rows of about three vectors per lane at 8 warps take one CTA of 16 warps per SM
+    # over short strips (T <= 12288), the pair layout of 8 warps above; other widths keep theirs
+    for H in (5632, 6144):
+        for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
+            short = rmsn.rmsn_plan(op, 12288, H, 1, 0)
+            long_ = rmsn.rmsn_plan(op, 12289, H, 1, 0)
+            assert (short["consumer_warps"], short["ctas_per_sm"]) == (16, 1)
+            assert (long_["consumer_warps"], long_["ctas_per_sm"]) == (8, 2)
+    for H in (4096, 5120):
+        assert rmsn.rmsn_plan(rmsn.OP_BWD, 4096, H, 1, 0)["consumer_warps"] == 8
+    assert rmsn.rmsn_plan(rmsn.OP_BWD, 4096, 6144, 0, 0)["consumer_warps"] == 16  # fp32 rows
+
+
+def test_plan_forward_rows_in_flight(lib):
+    # forward: 2 stages and 8 CTAs per SM for rows of at most 4 KiB, else one stage and
+    # about 48 KiB of rows in flight per SM
+    for H, xd, geom in [(1024, 1, (2, 8, 2)), (2048, 1, (2, 8, 2)), (4096, 1, (4, 6, 1)),
+                        (6144, 1, (4, 4, 1)), (8192, 1, (8, 3, 1)), (2048, 0, (4, 6, 1)),
+                        (4096, 0, (8, 3, 1)), (8192, 0, (8, 2, 1))]:
+        p = rmsn.rmsn_plan(rmsn.OP_FWD, 65536, H, xd, xd)
+        assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom, (H, xd, p)
 
 
 def test_workspace_grows_with_t(lib):

@@ -24,8 +24,10 @@ GEOMETRIES = [
     (1000, 2048, BF, F32, 4, 2, 4),
     (777, 4096, BF, BF, 8, 2, 2),
     (600, 5120, BF, F32, 8, 3, 2),
-    (600, 5632, BF, BF, 8, 3, 2),    # rows one at a time (third vector 3/4 full)
-    (555, 6144, BF, F32, 8, 3, 2),   # rows one at a time
+    (13000, 5632, BF, BF, 8, 3, 2),  # rows one at a time (third vector 3/4 full)
+    (12301, 6144, BF, F32, 8, 3, 2), # rows one at a time
+    (600, 5632, BF, BF, 16, 2, 1),   # the same widths over a short strip: 16 warps
+    (12288, 6144, BF, F32, 16, 2, 1),
     (1000, 8192, BF, BF, 16, 2, 1),
     (300, 16384, BF, F32, 16, 4, 1),
     (513, 4096, F32, F32, 16, 2, 1),
