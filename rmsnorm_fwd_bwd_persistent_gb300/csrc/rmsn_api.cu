@@ -131,7 +131,8 @@ int pick_nch(const int (&set)[N], int64_t need) {
 
 // The launch plan of one call.  Consumer warps: the smallest power of two (<= 8) whose
 // lanes hold about `target_nch` 16-byte vectors of a row each (the backward: 16 for rows
-// of at least 512 * target_nch vectors); the chunk variant is the
+// of at least 512 * target_nch vectors, and for some rows a count that is not a power of
+// two, below); the chunk variant is the
 // smallest compiled count that covers the row.  Shared memory per CTA: the ring header,
 // the weight vector, and as many stages (<= max_stages) as the CTA's share of the SM
 // holds (the backward at least two); fewer CTAs per SM if a share cannot hold two stages.
@@ -164,6 +165,23 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
         if (is_bwd && x_dt == RMSN_BF16 && nw == 8 && T <= 12288 &&
             cdiv(nvec, 32 * nw) == 3 && 4 * nvec >= 11 * 32 * (int64_t)nw)
             nw = 16;
+        // backward rows that the power of two above spreads thinly: the fewest warps that
+        // hold the row at target_nch vectors per lane, when those lanes are at least 7/8
+        // full and 16 / nb CTAs of them give at least 14 warps per SM (bf16 H 1344-1536,
+        // 2240-2560, 3136-3584; fp32 x at half those widths).  Where the power of two fills
+        // more than 5/8 of its lanes, only over long strips (T >= 16384): more chunks cost
+        // more than the fuller lanes save on short ones.  Measured on GB300, us per call:
+        // H 2304 (5 warps, 3 CTAs) at T = 8192: 37.2 -> 32.0, at 65536: 212 -> 163; H 2560
+        // at 4096: 25.9 -> 23.8, at 65536: 222 -> 167; H 1536 (3 warps, 5 CTAs) at 4096:
+        // 20.6 -> 22.4, at 65536: 117 -> 113; H 3584 (7 warps, 2 CTAs) at 4096: 27.9 -> 28.7,
+        // at 65536: 246 -> 229; H 3072 (6 warps, 12 per SM) was even, so it keeps 8.
+        if (is_bwd && nw <= 8) {
+            const int64_t nb = cdiv(nvec, 32 * P.target_nch);
+            const int64_t lanes = 32 * (int64_t)nw * cdiv(nvec, 32 * nw);  // at the power of two
+            if (nb < nw && 8 * nvec >= 7 * 32 * P.target_nch * nb &&
+                nb * (kWarpsPerSm / nb) >= 14 && (8 * nvec <= 5 * lanes || T >= 16384))
+                nw = (int)nb;
+        }
     }
     const int64_t need = cdiv(nvec, 32 * nw);
     int nch = 0;
@@ -371,8 +389,9 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
 int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages) {
     if (op < 0 || op >= kOps) return RMSN_ERR_INVALID_ARG;
     const bool is_bwd = op == RMSN_OP_BWD || op == RMSN_OP_BWD_RESIDUAL;
+    // the backward takes any number of consumer warps up to 16; the other kernels 1, 2, 4, 8
     if (consumer_warps < 0 || consumer_warps > (is_bwd ? 16 : 8) ||
-        (consumer_warps & (consumer_warps - 1)) != 0)
+        (!is_bwd && (consumer_warps & (consumer_warps - 1)) != 0))
         return RMSN_ERR_INVALID_ARG;
     if (ctas_per_sm < 0 || ctas_per_sm > 16 || max_stages < 0 || max_stages > 32)
         return RMSN_ERR_INVALID_ARG;

@@ -264,13 +264,12 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// True if any of the first nw (1, 2, 4, 8 or 16) "gave up" bytes at f (16-byte aligned) is
-// set.
+// True if any of the first nw (1 .. 16) "gave up" bytes at f (16-byte aligned) is set.
 __device__ __forceinline__ bool any_gave_up(const uint8_t* f, int nw) {
     const uint64_t* w = reinterpret_cast<const uint64_t*>(f);
-    if (nw >= 16) return (w[0] | w[1]) != 0;
-    const uint64_t mask = nw >= 8 ? ~0ull : ((1ull << (8 * nw)) - 1ull);
-    return (w[0] & mask) != 0;
+    auto bytes = [](int n) { return n >= 8 ? ~0ull : ((1ull << (8 * n)) - 1ull); };
+    if (nw <= 8) return (w[0] & bytes(nw)) != 0;
+    return (w[0] | (w[1] & bytes(nw - 8))) != 0;
 }
 
 // r[0] + r[1] + ... + r[nw-1], left to right, for nw in {1, 2, 4, 8} (r 16-byte aligned).
@@ -312,7 +311,8 @@ __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, i
 // lanes so that even lanes go on with v0 and odd lanes with v1; four more butterfly levels
 // among lanes of the same parity finish both warp sums (lane 0 holds v0's, lane 1 v1's).
 // Each warp posts its sums times m0 and m1 (rounded), and the posts are added in warp
-// order.  The order is fixed, so the bits depend only on the data.  nw is 1, 2, 4, 8 or 16.
+// order.  The order is fixed, so the bits depend only on the data.  nw is 1 .. 16 (the
+// powers of two read the posts as float4s; the order is the same either way).
 __device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v1, float m0,
                                               float m1, bool ok, int nw, int parity) {
     const int lane = threadIdx.x & 31;
@@ -355,6 +355,10 @@ __device__ __forceinline__ bool consumer_sum2(uint8_t* smem, float& v0, float& v
     } else {
         s0 = red[0];
         s1 = red[1];
+        for (int i = 1; i < nw; ++i) {
+            s0 = s0 + red[2 * i];
+            s1 = s1 + red[2 * i + 1];
+        }
     }
     v0 = s0;
     v1 = s1;

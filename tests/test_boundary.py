@@ -169,18 +169,52 @@ def test_plan_headline_geometry(lib):
 
 
 @pytest.mark.parametrize("H,xd,geom", [
-    (1536, 1, (4, 2, 4)), (2048, 1, (4, 2, 4)), (4096, 1, (8, 2, 2)), (5120, 1, (8, 3, 2)),
+    (1024, 1, (2, 2, 8)), (1536, 1, (3, 2, 5)), (2048, 1, (4, 2, 4)), (2560, 1, (5, 2, 3)),
+    (3072, 1, (8, 2, 2)), (3584, 1, (7, 2, 2)), (4096, 1, (8, 2, 2)), (5120, 1, (8, 3, 2)),
     (6144, 1, (8, 3, 2)), (8192, 1, (16, 2, 1)), (16384, 1, (16, 4, 1)),
-    (2048, 0, (8, 2, 2)), (4096, 0, (16, 2, 1)), (8192, 0, (16, 4, 1))])
+    (1280, 0, (5, 2, 3)), (2048, 0, (8, 2, 2)), (4096, 0, (16, 2, 1)), (8192, 0, (16, 4, 1))])
 def test_plan_backward_geometry_by_row_length(lib, H, xd, geom):
-    # 16 consumer warps per SM: 4 CTAs of 4 warps, 2 of 8, or one of 16 for rows of at
-    # least 1024 16-byte vectors; the residual backward plans the same way
+    # 14-16 consumer warps per SM: 8 CTAs of 2 warps, 4 of 4, 2 of 8, one of 16 for rows of
+    # at least 1024 16-byte vectors, or a count that is not a power of two (5 CTAs of 3,
+    # 3 of 5, 2 of 7) for rows those fill at two vectors per lane; the residual backward
+    # plans the same way
     for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
         p = rmsn.rmsn_plan(op, 65536, H, xd, 0)
         assert (p["consumer_warps"], p["chunks_per_lane"], p["ctas_per_sm"]) == geom
-        assert p["consumer_warps"] * p["ctas_per_sm"] == 16
+        assert 14 <= p["consumer_warps"] * p["ctas_per_sm"] <= 16
         assert p["grid"] == SM * p["ctas_per_sm"]
         assert p["workspace_bytes"] == 8 * H * p["grid"]
+
+
+def test_plan_backward_warps_not_a_power_of_two(lib):
+    # every width that takes a warp count other than a power of two: the row fills those
+    # warps at two vectors per lane to at least 7/8, the power of two would have been
+    # larger, and the SM holds at least 14 of the warps
+    seen = set()
+    for xd, vec in ((1, 8), (0, 4)):
+        for H in range(vec, (16384 if xd else 8192) + 1, vec):  # fp32 rows up to 8192
+            p = rmsn.rmsn_plan(rmsn.OP_BWD, 65536, H, xd, 0)
+            nw, nvec = p["consumer_warps"], H // vec
+            assert p["chunks_per_lane"] * 32 * nw >= nvec
+            if nw & (nw - 1) == 0:
+                continue
+            seen.add(nw)
+            assert p["chunks_per_lane"] == 2 and 8 * nvec >= 7 * 64 * nw and nvec <= 64 * nw
+            assert nw * p["ctas_per_sm"] >= 14
+            assert 1 << (nw - 1).bit_length() > nw  # the power of two it replaces
+            assert rmsn.rmsn_plan(rmsn.OP_BWD_RESIDUAL, 65536, H, xd, 0)["consumer_warps"] == nw
+    assert seen == {3, 5, 7}
+
+
+def test_plan_backward_warps_not_a_power_of_two_by_strip_length(lib):
+    # rows the power of two fills to more than 5/8 (bf16 H 1536, 3584) change only over long
+    # strips (T >= 16384); rows it fills to at most 5/8 (bf16 H 2304-2560, fp32 H 1280) at any T
+    for H, xd, nw, nb in ((1536, 1, 4, 3), (3584, 1, 8, 7)):
+        for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
+            assert rmsn.rmsn_plan(op, 16383, H, xd, 0)["consumer_warps"] == nw
+            assert rmsn.rmsn_plan(op, 16384, H, xd, 0)["consumer_warps"] == nb
+    for H, xd in ((2304, 1), (2560, 1), (1280, 0)):
+        assert rmsn.rmsn_plan(rmsn.OP_BWD, 300, H, xd, 0)["consumer_warps"] == 5
 
 
 def test_plan_backward_short_strip_rule(lib):
@@ -240,7 +274,15 @@ def test_set_policy_backward_sixteen_warps(lib):
     with pytest.raises(rmsn.RmsnError):
         rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=32)
     with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=17)
+    with pytest.raises(rmsn.RmsnError):
+        rmsn.rmsn_set_policy(rmsn.OP_FWD_RESIDUAL, consumer_warps=6)
+    try:  # any count up to 16 for the backward
         rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=12)
+        p = rmsn.rmsn_plan(rmsn.OP_BWD, 8192, 4096, 1, 1)
+        assert (p["consumer_warps"], p["threads"], p["chunks_per_lane"]) == (12, 384, 2)
+    finally:
+        rmsn.rmsn_set_policy(rmsn.OP_BWD)
     for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
         try:
             rmsn.rmsn_set_policy(op, consumer_warps=16)

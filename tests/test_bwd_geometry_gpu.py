@@ -1,7 +1,8 @@
 """GPU parity of the strip backward in every class of launch geometry its plan picks (T
 above the small-T route, so the deterministic calls run the strip kernel and the column
 reduce):
-4 CTAs of 4 warps, 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
+4 CTAs of 4 warps, 5 of 3, 3 of 5 and 2 of 7 (rows that fill those warps at two vectors
+per lane), 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
 2 CTAs of 8 warps with rows one at a time (bf16, about three vectors per lane) and one CTA
 of 16 warps (rows of at least 1024 vectors), each against the FP64 oracle, with plain and
 TwoSum-compensated dW, for rmsnorm_bwd and rmsnorm_bwd_residual (FlashInfer PR #5741
@@ -22,6 +23,11 @@ BF, F32 = torch.bfloat16, torch.float32
 # (T, H, x dtype, w dtype, consumer warps, vectors per lane, CTAs per SM)
 GEOMETRIES = [
     (1000, 2048, BF, F32, 4, 2, 4),
+    (16401, 1536, BF, F32, 3, 2, 5),   # long strips only
+    (901, 2560, BF, BF, 5, 2, 3),
+    (700, 2304, BF, F32, 5, 2, 3),     # last lanes' second vector empty
+    (16390, 3584, BF, F32, 7, 2, 2),   # long strips only
+    (900, 1280, F32, F32, 5, 2, 3),
     (777, 4096, BF, BF, 8, 2, 2),
     (600, 5120, BF, F32, 8, 3, 2),
     (13000, 5632, BF, BF, 8, 3, 2),  # rows one at a time (third vector 3/4 full)

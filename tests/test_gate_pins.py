@@ -223,7 +223,8 @@ def _rows(H, n_rand, n_cancel, seed, x_bf16=True, w_bf16=True):
 
 # (H, consumer warps, vectors per lane) as the planner picks them for the strip kernel,
 # and the small-T kernel's fixed 256-thread row task
-GEOMETRIES = [(256, 1, 1, False), (1536, 4, 2, False), (4096, 8, 2, False),
+GEOMETRIES = [(256, 1, 1, False), (1536, 3, 2, False), (2048, 4, 2, False),
+              (2560, 5, 2, False), (3584, 7, 2, False), (4096, 8, 2, False),
               (6144, 8, 3, False), (4096, 8, 2, True)]
 
 
