@@ -78,13 +78,13 @@ __device__ __forceinline__ f2 f2_make(float lo, float hi) {
 }
 __device__ __forceinline__ f2 f2_splat(float v) { return f2_make(v, v); }
 __device__ __forceinline__ float f2_lo(f2 v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    float lo;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
     return lo;
 }
 __device__ __forceinline__ float f2_hi(f2 v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    float hi;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
     return hi;
 }
 __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
