@@ -43,7 +43,8 @@ def ulp_bf16(ref: np.ndarray) -> np.ndarray:
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16)
-    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns widen to quiet NaNs
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def check_bf16(dev_bits: np.ndarray, ref: np.ndarray, extra: np.ndarray | None = None) -> dict:
