@@ -88,6 +88,9 @@ const char* rmsn_status_string(int status);
  *         the product formed in FP32 left to right and rounded once
  *   rstd  [T] fp32 (device, written); rstd_i = 1 / sqrt(sum_j x_ij^2 / H + eps)
  *   eps   finite, >= 0 (with eps == 0 an all-zero row gives rstd = inf)
+ * The sum of squares is FP32, as the source states: a row whose sum of squares leaves the
+ * FP32 range (finite elements of magnitude above about 1.8e19 / sqrt(H)) gets rstd = 0 and
+ * y = 0, and its backward gives dx = 0 and no dW term.
  * Returns RMSN_OK or an error status (see conventions).
  * ---------------------------------------------------------------------------------- */
 int rmsnorm_fwd(const void* x, int x_dtype, const void* w, int w_dtype, void* y, float* rstd,

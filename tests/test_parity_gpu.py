@@ -126,6 +126,27 @@ def test_bwd_special_rows():
     P.assert_ok(P.check_bwd(dy, x, w, rstd), "special rows")
 
 
+@pytest.mark.parametrize("T", [5, 300])  # the small-T route and the strip kernel
+def test_row_beyond_fp32_range(T):
+    # a row whose FP32 sum of squares overflows: rstd = 1/sqrt(inf) = 0 and y = 0 (the
+    # pages' FP32 sum of squares; the FP64 oracle does not overflow there, so the forward of
+    # the other rows is compared with it separately); the backward at the saved rstd gives
+    # dx = 0 for that row and adds nothing to dW, which the oracle at the same rstd confirms
+    H = 1024
+    x, dy, w = wl.fwd_bwd_inputs(_wl(wl.MAIN_BF16, T, H), DEV, seed=12)
+    x[2] = 1e20
+    y, rstd = rmsn.rmsnorm_fwd(x, w, 1e-6)
+    dx, dw = rmsn.rmsnorm_bwd(dy, x, w, rstd)
+    torch.cuda.synchronize()
+    assert rstd[2].item() == 0.0
+    assert bool((y[2] == 0).all()) and bool((dx[2] == 0).all())
+    keep = torch.tensor([i for i in range(T) if i != 2], device=DEV)
+    P.assert_ok(P.check_fwd(x[keep].contiguous(), w, 1e-6), "forward of the other rows")
+    P.assert_ok(P.gate_bwd(dy, x, w, rstd, dx, dw, deterministic=True, all_rows=True),
+                "backward at the saved rstd")
+    assert rmsn.rmsn_device_status() == 0
+
+
 def test_bwd_t0_zeroes_dw():
     x = torch.empty(0, 256, device=DEV, dtype=torch.bfloat16)
     w = torch.ones(256, device=DEV, dtype=torch.bfloat16)
