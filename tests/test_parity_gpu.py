@@ -126,6 +126,44 @@ def test_bwd_special_rows():
     P.assert_ok(P.check_bwd(dy, x, w, rstd), "special rows")
 
 
+@pytest.mark.parametrize("T,H,xd,wd", [(300, 4096, torch.bfloat16, torch.bfloat16),
+                                       (700, 1536, torch.bfloat16, torch.float32),
+                                       (65, 2048, torch.bfloat16, torch.float32),
+                                       (257, 2048, torch.float32, torch.float32)])
+def test_forward_then_backward_at_the_oracles_rstd(T, H, xd, wd):
+    # end to end: the device's forward and then its backward (at the rstd the forward saved),
+    # against the oracle's own chain (its FP64 rstd, then the backward at that rstd).  Beyond
+    # the usual gates, dx may move by |d(dx)/d(rstd)| * |rstd_dev - rstd_ref| with
+    # d(dx)/d(rstd) = g - 3 rstd^2 x mean(g x), bounded per element
+    from oracle import gates
+    import oracle
+    x, dy, w = wl.fwd_bwd_inputs(_wl(wl.MAIN_BF16, T, H, xd, wd), DEV, seed=T + H)
+    _, rstd = rmsn.rmsnorm_fwd(x, w, 1e-6)
+    dx, dw = rmsn.rmsnorm_bwd(dy, x, w, rstd)
+    torch.cuda.synchronize()
+    X, DY, W = wl.to_oracle(x), wl.to_oracle(dy), wl.to_oracle(w)
+    _, r_ref = oracle.rmsnorm_fwd(X, W, 1e-6)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(DY, X, W, r_ref)
+    r_dev = rstd.cpu().numpy().astype(np.float64)
+    assert gates.check_f32_rel(r_dev, r_ref)["n_fail"] == 0
+    dec = oracle.bf16_bits_to_f64 if xd == torch.bfloat16 else (lambda a: np.asarray(a, np.float64))
+    decw = oracle.bf16_bits_to_f64 if wd == torch.bfloat16 else (lambda a: np.asarray(a, np.float64))
+    xf, dyf, wf = dec(X), dec(DY), decw(W)
+    g = dyf * wf[None, :]
+    S = np.mean(g * xf, axis=1, keepdims=True)
+    dr = np.abs(r_dev - r_ref)[:, None]
+    r = np.maximum(r_dev, r_ref)[:, None]
+    moved = 1.01 * dr * (np.abs(g) + 3.0 * r * r * np.abs(xf) * np.abs(S))
+    if xd == torch.bfloat16:
+        depth = P.row_dot_depth(T, H, xd, wd, True)
+        extra = gates.dx_fp32_bound(dyf, xf, wf, r_dev, dx_ref, depth) + moved
+        res = gates.check_bf16(wl.to_oracle(dx), dx_ref, extra=extra)
+    else:
+        res = gates.check_f32_rel(wl.to_oracle(dx), dx_ref, row_rms_term=True)
+    assert res["n_fail"] == 0, res
+    assert gates.check_dw(dw.cpu().numpy(), dw_ref)["n_fail"] == 0
+
+
 @pytest.mark.parametrize("T", [5, 300])  # the small-T route and the strip kernel
 def test_row_beyond_fp32_range(T):
     # a row whose FP32 sum of squares overflows: rstd = 1/sqrt(inf) = 0 and y = 0 (the
