@@ -24,6 +24,7 @@ MAX_WIDENED_ROW_ULP = 1.0  # and their error, in bf16 ulps of the row's RMS
 # Widening statistics of every bf16 dx gate evaluated in this process (printed by the
 # terminal summary in conftest.py).
 WIDENING: list = []
+DW_BUDGET: list = []  # every dW comparison: worst |dw - ref| / (1e-4 + 1e-4 |ref|), rel-L2
 
 
 def guarded(shape, dtype, device, fill=float("nan")):
@@ -110,6 +111,12 @@ def _widening(r: dict, what: str) -> dict:
             "max_widened_err_row_ulp": r["max_widened_err_row_ulp"]}
 
 
+def _dw_record(r: dict, what: str) -> dict:
+    """Records a dW comparison's budget figures for the end-of-run summary."""
+    DW_BUDGET.append({"what": what, "n": r["n"], "worst": r["worst"], "rel_l2": r["rel_l2"]})
+    return r
+
+
 def _f64(a: np.ndarray) -> np.ndarray:
     return oracle.bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
 
@@ -167,7 +174,8 @@ def gate_bwd(dy, x, w, rstd, dx, dw, deterministic: bool, all_rows: bool = False
         out["dx_widening"] = _widening(out["dx"], f"bwd T={T} H={H} det={int(deterministic)}")
     if full_dw:
         _, dw_ref = oracle.rmsnorm_bwd(wl.to_oracle(dy), wl.to_oracle(x), W, r_all, want_dx=False)
-        out["dw"] = gates.check_dw(dw.cpu().numpy(), dw_ref)
+        out["dw"] = _dw_record(gates.check_dw(dw.cpu().numpy(), dw_ref),
+                               f"bwd T={T} H={H} det={int(deterministic)}")
     return out
 
 
@@ -259,7 +267,7 @@ def check_bwd_residual(dy, h, w, rstd, g_res, deterministic=True, compensated=Fa
         out["dx_total"] = gates.check_f32_rel(dx_dev, dxt_ref, row_rms_term=True)
     _, dw_ref = oracle.rmsnorm_bwd_residual(wl.to_oracle(dy_in), wl.to_oracle(h), W, r_all,
                                             wl.to_oracle(g_in), want_dx=False)
-    out["dw"] = gates.check_dw(dw.cpu().numpy(), dw_ref)
+    out["dw"] = _dw_record(gates.check_dw(dw.cpu().numpy(), dw_ref), f"bwd_residual T={T} H={H}")
     bufs = [dwbuf] + ([dxbuf] if dxbuf is not None else [])
     out["guards"] = {"n_fail": int(not all(guards_ok(b) for b in bufs))}
     out["device_status"] = {"n_fail": rmsn.rmsn_device_status()}

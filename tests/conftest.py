@@ -28,8 +28,17 @@ def pytest_collection_modifyitems(config, items):
 
 def pytest_terminal_summary(terminalreporter, exitstatus, config):
     """Widening statistics of the bf16 dx gates (elements that needed the a-priori FP32
-    bound on top of one ulp, and their error in bf16 ulps of their row's RMS)."""
+    bound on top of one ulp, and their error in bf16 ulps of their row's RMS), and the
+    weight-gradient budget figures of every dW comparison."""
     mod = sys.modules.get("_parity")
+    dwr = getattr(mod, "DW_BUDGET", None) if mod else None
+    if dwr:
+        tr = terminalreporter
+        w = max(dwr, key=lambda r: r["worst"])
+        tr.section("dW budget")
+        tr.write_line(f"{len(dwr)} dW comparisons, {sum(r['n'] for r in dwr)} elements: worst "
+                      f"|dw - ref| / (1e-4 + 1e-4 |ref|) = {w['worst']:.4f} (limit 1) at "
+                      f"{w['what']}; max rel-L2 {max(r['rel_l2'] for r in dwr):.2e}")
     rec = getattr(mod, "WIDENING", None) if mod else None
     if not rec:
         return
