@@ -42,6 +42,10 @@ struct Policy {
 // a launch-policy sweep on GB300 (bf16 and fp32, H 1024-8192, T 8192 and 65536) found the
 // best CTAs per SM at about this many bytes of rows in flight, with one stage per CTA.
 constexpr int64_t kFwdBytesInFlight = 48 << 10;
+// The fused quant: stage bytes in flight per SM it aims for, and the warps per SM its
+// register file holds at the kernel's bound of 72 registers per thread.
+constexpr int64_t kFusedBytesInFlight = 64 << 10;
+constexpr int64_t kFusedWarpsPerSm = 65536 / (72 * 32);
 
 // Per op: FWD, BWD, FUSED, FWD_RESIDUAL, BWD_RESIDUAL.
 constexpr int kOps = 5;
@@ -49,7 +53,8 @@ constexpr Policy kDefaultPolicy[kOps] = {
     {0, 0, 0, 6, 16},  // forward: at least 2 warps, about 6 vectors per lane, CTAs and
                        // stages from the row size
     {0, 0, 4, 2, 8},   // backward: 8 consumer warps at bf16 H 4096-6144, 16 per SM in all
-    {0, 3, 1, 2, 8},   // fused quant: 8 consumer warps at H >= 4096, 3 CTAs per SM, one stage
+    {0, 0, 1, 3, 8},   // fused quant: at most 3 vectors per lane, one stage, CTAs from the
+                       // row size
     {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
     {0, 0, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
 };
@@ -208,6 +213,18 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
         cps = small_rows ? 8
                          : (int)std::max<int64_t>(2, std::min<int64_t>(
                                8, (kFwdBytesInFlight + row_bytes / 2) / row_bytes));
+    // the fused quant (one stage per CTA): about kFusedBytesInFlight of stages per SM, at
+    // least two CTAs, at most as many as the registers hold.  Measured on GB300 at T = 8192
+    // / 32768 against 3 CTAs of 2-8 warps at two vectors per lane: H 1024 34.2 -> 20.6 /
+    // 110.8 -> 56.2 us (2 warps, 9 CTAs), H 2048 38.6 -> 30.3 / 129.0 -> 100.8 (4 warps,
+    // 5 CTAs), H 3072 49.0 -> 41.1 / 169.4 -> 150.2 (4 warps, 5 CTAs), H 12288 246.6 ->
+    // 162.3 / 951.5 -> 614.3 (2 CTAs, was 1); H 4096-8192 keep their plans (3 CTAs of 8
+    // warps up to H 6144, 2 at H 8192, where 3 were 3-9% slower).
+    if (cps == 0 && op == RMSN_OP_FUSED_QUANT) {
+        const int64_t by_bytes = (kFusedBytesInFlight + stage_bytes / 2) / stage_bytes;
+        const int64_t by_regs = kFusedWarpsPerSm / (nw + 1);  // + the producer warp
+        cps = (int)std::max<int64_t>(2, std::min(by_bytes, by_regs));
+    }
     if (cps == 0) cps = nw >= kWarpsPerSm ? 1 : kWarpsPerSm / nw;
     const int max_stages = P.max_stages > 0 ? P.max_stages : (small_rows ? 2 : 1);
     auto stages_for = [&](int c) -> int64_t {
@@ -217,9 +234,11 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     };
     // the backward holds two rows' stages at once (it takes rows two at a time)
     const int64_t min_stages = is_bwd ? 2 : 1;
-    // room for two stages per CTA (the forward: for as many as it will use)
-    const int64_t want_stages =
-        op == RMSN_OP_FWD ? std::max<int64_t>(1, std::min<int64_t>(2, max_stages)) : 2;
+    // room for two stages per CTA (the forward and the fused quant: for as many as they
+    // will use)
+    const int64_t want_stages = (op == RMSN_OP_FWD || op == RMSN_OP_FUSED_QUANT)
+                                    ? std::max<int64_t>(1, std::min<int64_t>(2, max_stages))
+                                    : 2;
     while (cps > 1 && stages_for(cps) < want_stages) --cps;
     int64_t stages = stages_for(cps);
     if (stages < min_stages) return RMSN_ERR_UNSUPPORTED_SHAPE;

@@ -241,6 +241,20 @@ def test_plan_forward_rows_in_flight(lib):
         assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom, (H, xd, p)
 
 
+def test_plan_fused_rows_in_flight(lib):
+    # the fused quant: at most three vectors per lane; one stage per CTA; about 64 KiB of
+    # stages in flight per SM, at least 2 CTAs, at most the CTAs whose warps (with the
+    # producer) the register file holds at 72 registers per thread; fewer where shared
+    # memory runs out
+    for H, geom in [(512, (1, 14)), (1024, (2, 9)), (1536, (2, 9)), (2048, (4, 5)),
+                    (3072, (4, 5)), (4096, (8, 3)), (6144, (8, 3)), (8192, (8, 2)),
+                    (12288, (8, 2)), (16384, (8, 1))]:
+        p = rmsn.rmsn_plan(rmsn.OP_FUSED_QUANT, 65536, H, 1, 1)
+        assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom + (1,), (H, p)
+        assert p["chunks_per_lane"] <= 8 and p["chunks_per_lane"] * 32 * p["consumer_warps"] >= H // 8
+        assert (p["consumer_warps"] + 1) * p["ctas_per_sm"] <= 65536 // (72 * 32)
+
+
 def test_workspace_grows_with_t(lib):
     prev = 0
     for T in (1, 2, 3, 17, 100, 1000, 10 ** 4, 10 ** 5, 10 ** 6):
