@@ -55,7 +55,7 @@ constexpr Policy kDefaultPolicy[kOps] = {
     {0, 0, 4, 2, 8},   // backward: 8 consumer warps at bf16 H 4096-6144, 16 per SM in all
     {0, 0, 1, 3, 8},   // fused quant: at most 3 vectors per lane, one stage, CTAs from the
                        // row size
-    {0, 4, 2, 4, 16},  // residual forward: as the forward, two rows per stage
+    {0, 0, 2, 4, 16},  // residual forward: as the forward, two rows per stage
     {0, 0, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
 };
 Policy g_policy[kOps] = {kDefaultPolicy[0], kDefaultPolicy[1], kDefaultPolicy[2],
@@ -209,6 +209,10 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     // run out (the grid is clamped to the resident CTAs at launch)
     const bool small_rows = row_bytes <= 4096;
     int cps = P.ctas_per_sm;
+    // the residual forward (two rows per stage, two stages): 8 CTAs for rows of at most
+    // 4 KiB, else 4.  Measured on GB300 at T = 8192 / 32768 against 4 CTAs: H 512 16.4 ->
+    // 12.8 / 41.7 -> 28.7 us, H 1024 20.4 -> 16.5 / 59.4 -> 45.0, H 2048 even
+    if (cps == 0 && op == RMSN_OP_FWD_RESIDUAL) cps = small_rows ? 8 : 4;
     if (cps == 0 && op == RMSN_OP_FWD)
         cps = small_rows ? 8
                          : (int)std::max<int64_t>(2, std::min<int64_t>(

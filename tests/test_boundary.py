@@ -241,6 +241,15 @@ def test_plan_forward_rows_in_flight(lib):
         assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom, (H, xd, p)
 
 
+def test_plan_residual_forward_rows_in_flight(lib):
+    # the residual forward: 8 CTAs per SM for rows of at most 4 KiB, else 4 (fewer where
+    # shared memory runs out), two stages
+    for H, xd, cps in [(512, 1, 8), (1024, 1, 8), (2048, 1, 8), (1024, 0, 8), (3072, 1, 4),
+                       (4096, 1, 4), (2048, 0, 4), (8192, 1, 2), (16384, 1, 1)]:
+        p = rmsn.rmsn_plan(rmsn.OP_FWD_RESIDUAL, 65536, H, xd, xd)
+        assert (p["ctas_per_sm"], p["stages"]) == (cps, 2), (H, xd, p)
+
+
 def test_plan_fused_rows_in_flight(lib):
     # the fused quant: at most three vectors per lane; one stage per CTA; about 64 KiB of
     # stages in flight per SM, at least 2 CTAs, at most the CTAs whose warps (with the
