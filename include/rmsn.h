@@ -289,7 +289,8 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
               int sm_count, rmsn_plan_t* out);
 
 /* Tuning hook for benchmarks: overrides the consumer warps per CTA (a power of two
- * <= 8; any count <= 16 for the two backward ops), the CTAs per SM and the maximum ring depth of
+ * <= 8, or 16 for the fused quant; any count <= 16 for the two backward ops), the CTAs per
+ * SM and the maximum ring depth of
  * one op for the whole process (0 keeps a default).  The backward's chunk count, and so its dw bits, follow the CTAs
  * per SM; rmsnorm_bwd_workspace_bytes reflects the current setting.  Changing it while
  * calls are in flight on other host threads is a race.  Returns RMSN_ERR_INVALID_ARG for

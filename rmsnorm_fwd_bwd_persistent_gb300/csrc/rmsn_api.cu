@@ -53,8 +53,8 @@ constexpr Policy kDefaultPolicy[kOps] = {
     {0, 0, 0, 6, 16},  // forward: at least 2 warps, about 6 vectors per lane, CTAs and
                        // stages from the row size
     {0, 0, 4, 2, 8},   // backward: 8 consumer warps at bf16 H 4096-6144, 16 per SM in all
-    {0, 0, 1, 3, 8},   // fused quant: at most 3 vectors per lane, one stage, CTAs from the
-                       // row size
+    {0, 0, 0, 3, 8},   // fused quant: at most 3 vectors per lane (16 warps for the longest
+                       // rows), stages and CTAs from the row size
     {0, 0, 2, 4, 16},  // residual forward: as the forward, two rows per stage
     {0, 0, 4, 2, 8},   // residual backward: as the backward (g_residual from global memory)
 };
@@ -163,6 +163,11 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
         // backward rows that fill 16 warps at target_nch vectors per lane take 16 warps
         // (one CTA per SM), so every lane keeps its share of a row pair in registers
         if (is_bwd && nvec >= 16 * 32 * P.target_nch) nw = 16;
+        // the fused quant: rows of more than 1024 vectors (bf16 H > 8192) take one CTA of 16
+        // warps per SM (the 8-warp kernel would hold 4-8 vectors per lane and spill).
+        // Measured on GB300 at T = 8192 / 32768: H 10240 159 -> 139 / 605 -> 526 us, H 12288
+        // 162 -> 143 / 618 -> 549, H 16384 338 -> 193 / 1314 -> 739; H 8192 keeps 2 CTAs of 8
+        if (op == RMSN_OP_FUSED_QUANT && nvec > 1024) nw = 16;
         // bf16 rows of about three vectors per lane at 8 warps (H 5632-6144) over a short
         // strip: one CTA of 16 warps per SM is faster up to T ~ 12288 (measured on GB300:
         // 14-16% at T = 2048, 8-9% at 4096, 2-4% at 8192, even at 16384, slower above), its
@@ -224,13 +229,19 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     // 5 CTAs), H 3072 49.0 -> 41.1 / 169.4 -> 150.2 (4 warps, 5 CTAs), H 12288 246.6 ->
     // 162.3 / 951.5 -> 614.3 (2 CTAs, was 1); H 4096-8192 keep their plans (3 CTAs of 8
     // warps up to H 6144, 2 at H 8192, where 3 were 3-9% slower).
+    if (cps == 0 && op == RMSN_OP_FUSED_QUANT && nw > 8) cps = 1;  // 16 warps: one CTA
     if (cps == 0 && op == RMSN_OP_FUSED_QUANT) {
         const int64_t by_bytes = (kFusedBytesInFlight + stage_bytes / 2) / stage_bytes;
         const int64_t by_regs = kFusedWarpsPerSm / (nw + 1);  // + the producer warp
         cps = (int)std::max<int64_t>(2, std::min(by_bytes, by_regs));
     }
     if (cps == 0) cps = nw >= kWarpsPerSm ? 1 : kWarpsPerSm / nw;
-    const int max_stages = P.max_stages > 0 ? P.max_stages : (small_rows ? 2 : 1);
+    // the fused quant's 16-warp CTA: two stages while they stay within about 96 KiB (H up
+    // to 12288: 143 against 155 us at T = 8192), else one (H 16384: 193 against 199)
+    const int max_stages =
+        P.max_stages > 0 ? P.max_stages
+        : (op == RMSN_OP_FUSED_QUANT) ? (nw > 8 && stage_bytes <= (96 << 10) / 2 ? 2 : 1)
+        : (small_rows ? 2 : 1);
     auto stages_for = [&](int c) -> int64_t {
         int64_t share = smem_sm / c - kSmemReservedPerCta;
         if (share > smem_cta) share = smem_cta;
@@ -412,8 +423,10 @@ int rmsn_plan(int op, int64_t T, int64_t H, int x_dtype, int w_dtype, int compen
 int rmsn_set_policy(int op, int consumer_warps, int ctas_per_sm, int max_stages) {
     if (op < 0 || op >= kOps) return RMSN_ERR_INVALID_ARG;
     const bool is_bwd = op == RMSN_OP_BWD || op == RMSN_OP_BWD_RESIDUAL;
-    // the backward takes any number of consumer warps up to 16; the other kernels 1, 2, 4, 8
-    if (consumer_warps < 0 || consumer_warps > (is_bwd ? 16 : 8) ||
+    // the backward takes any number of consumer warps up to 16, the fused quant 1, 2, 4, 8
+    // or 16 (16 for rows of 1024-2048 vectors), the forwards 1, 2, 4, 8
+    const int max_warps = (is_bwd || op == RMSN_OP_FUSED_QUANT) ? 16 : 8;
+    if (consumer_warps < 0 || consumer_warps > max_warps ||
         (!is_bwd && (consumer_warps & (consumer_warps - 1)) != 0))
         return RMSN_ERR_INVALID_ARG;
     if (ctas_per_sm < 0 || ctas_per_sm > 16 || max_stages < 0 || max_stages > 32)

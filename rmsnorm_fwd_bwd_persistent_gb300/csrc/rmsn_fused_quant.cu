@@ -109,8 +109,10 @@ __device__ __forceinline__ uint2 quotient_codes(const f2 (&n)[4], float y, float
     return make_uint2(e4m3x4(qd[0], qd[1]), e4m3x4(qd[2], qd[3]));
 }
 
-template <int NCH>
-__global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs a) {
+// MAXT / MINB: the launch bound (8 consumer warps + producer at 3 CTAs per SM, 72 registers
+// per thread; or 16 + producer at one CTA per SM for long rows, 120 registers).
+template <int NCH, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) fused_add_rmsnorm_fp8_kernel(FusedArgs a) {
     constexpr int VEC = 8;
     extern __shared__ __align__(128) uint8_t smem[];
     const Ring ring = ring_at(smem, a.stages, a.stage_bytes, a.data_off);
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
         }
         if (__all_sync(0xffffffffu, ok)) ring_release(ring, at);
         float ss = __fadd_rn(f2_lo(ss2), f2_hi(ss2));
-        if (!consumer_sum(smem, ss, ok, nw, (int)(k & 1))) break;
+        if (!consumer_sum<(MAXT > 288 ? 16 : 8)>(smem, ss, ok, nw, (int)(k & 1))) break;
         const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), a.eps)));
         const f2 rs2 = f2_splat(rs);
 
@@ -222,9 +224,9 @@ __global__ void __launch_bounds__(288, 3) fused_add_rmsnorm_fp8_kernel(FusedArgs
     }
 }
 
-template <int NCH>
+template <int NCH, int MAXT = 288, int MINB = 3>
 static cudaError_t run(const Launch& L, const FusedArgs& a, cudaStream_t s) {
-    auto k = fused_add_rmsnorm_fp8_kernel<NCH>;
+    auto k = fused_add_rmsnorm_fp8_kernel<NCH, MAXT, MINB>;
     const int threads = L.nw * 32 + 32;
     int64_t grid = 0;
     cudaError_t e = fit_grid((const void*)k, L, threads, &grid);
@@ -240,6 +242,14 @@ cudaError_t launch_fused(const Launch& L, const void* x, void* residual, const v
                 static_cast<const __nv_bfloat16*>(w), q, block_scale,
                 static_cast<__nv_bfloat16*>(normed), L.err, T, scale_ld, L.limit_ns, (int)H,
                 L.nw, L.stages, L.row_bytes, L.stage_bytes, L.w_bytes, L.data_off, eps};
+    if (L.nw > 8) {  // 16 consumer warps: rows of 1024-2048 vectors
+        switch (L.nch) {
+            case 2: return run<2, 544, 1>(L, a, s);
+            case 3: return run<3, 544, 1>(L, a, s);
+            case 4: return run<4, 544, 1>(L, a, s);
+            default: return cudaErrorInvalidConfiguration;
+        }
+    }
     switch (L.nch) {
         case 1: return run<1>(L, a, s);
         case 2: return run<2>(L, a, s);

@@ -272,14 +272,23 @@ __device__ __forceinline__ bool any_gave_up(const uint8_t* f, int nw) {
     return (w[0] | (w[1] & bytes(nw - 8))) != 0;
 }
 
-// r[0] + r[1] + ... + r[nw-1], left to right, for nw in {1, 2, 4, 8} (r 16-byte aligned).
+// r[0] + r[1] + ... + r[nw-1], left to right, for nw in {1, 2, 4, 8} and, when MAXW is
+// 16, also 16 (r 16-byte aligned).
+template <int MAXW = 8>
 __device__ __forceinline__ float sum_posts(const float* r, int nw) {
     if (nw >= 4) {
         const float4 a = *reinterpret_cast<const float4*>(r);
         float s = a.x + a.y + a.z + a.w;
-        if (nw == 8) {
+        if (nw == 8 || (MAXW >= 16 && nw == 16)) {
             const float4 b = *reinterpret_cast<const float4*>(r + 4);
             s = s + b.x + b.y + b.z + b.w;
+        }
+        if constexpr (MAXW >= 16) {
+            if (nw == 16) {
+                const float4 c = *reinterpret_cast<const float4*>(r + 8);
+                const float4 d = *reinterpret_cast<const float4*>(r + 12);
+                s = s + c.x + c.y + c.z + c.w + d.x + d.y + d.z + d.w;
+            }
         }
         return s;
     }
@@ -290,6 +299,7 @@ __device__ __forceinline__ float sum_posts(const float* r, int nw) {
 // vote: every consumer warp reduces its value by a butterfly of shuffles and posts it with
 // whether its wait succeeded, one named barrier, then every lane adds the posts in warp
 // order (same bits on every lane).  Returns false if any consumer warp gave up on this row.
+template <int MAXW = 8>
 __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, int nw,
                                              int parity) {
 #pragma unroll
@@ -303,7 +313,7 @@ __device__ __forceinline__ bool consumer_sum(uint8_t* smem, float& v, bool ok, i
         ab[warp] = warp_ok ? 0 : 1;
     }
     named_bar(1, nw * 32);
-    v = sum_posts(red, nw);
+    v = sum_posts<MAXW>(red, nw);
     return !any_gave_up(ab, nw);
 }
 

@@ -139,7 +139,8 @@ def test_plan_covers_rows(lib, op, H, xd, wd):
         assert p["vec_elems"] == vec
         assert p["chunks_per_lane"] * lanes * vec >= H              # the row is covered
         producer = 0 if is_bwd else 32                              # bwd: thread 0 feeds the ring
-        assert p["threads"] == lanes + producer and p["threads"] <= (512 if is_bwd else 288)
+        max_threads = 512 if is_bwd else (544 if op == rmsn.OP_FUSED_QUANT else 288)
+        assert p["threads"] == lanes + producer and p["threads"] <= max_threads
         assert 1 <= p["grid"] <= min(T, SM * p["ctas_per_sm"])      # every CTA has a row
         row = H * (2 if xd == 1 else 4)
         rows = 1 if op == rmsn.OP_FWD else 2                        # rows per stage
@@ -255,13 +256,19 @@ def test_plan_fused_rows_in_flight(lib):
     # stages in flight per SM, at least 2 CTAs, at most the CTAs whose warps (with the
     # producer) the register file holds at 72 registers per thread; fewer where shared
     # memory runs out
-    for H, geom in [(512, (1, 14)), (1024, (2, 9)), (1536, (2, 9)), (2048, (4, 5)),
-                    (3072, (4, 5)), (4096, (8, 3)), (6144, (8, 3)), (8192, (8, 2)),
-                    (12288, (8, 2)), (16384, (8, 1))]:
+    # memory runs out; rows of more than 1024 vectors: one CTA of 16 warps, two stages up to
+    # 48 KiB each
+    for H, geom in [(512, (1, 14, 1)), (1024, (2, 9, 1)), (1536, (2, 9, 1)), (2048, (4, 5, 1)),
+                    (3072, (4, 5, 1)), (4096, (8, 3, 1)), (6144, (8, 3, 1)), (8192, (8, 2, 1)),
+                    (8320, (16, 1, 2)), (12288, (16, 1, 2)), (12416, (16, 1, 1)),
+                    (16384, (16, 1, 1))]:
         p = rmsn.rmsn_plan(rmsn.OP_FUSED_QUANT, 65536, H, 1, 1)
-        assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom + (1,), (H, p)
+        assert (p["consumer_warps"], p["ctas_per_sm"], p["stages"]) == geom, (H, p)
         assert p["chunks_per_lane"] <= 8 and p["chunks_per_lane"] * 32 * p["consumer_warps"] >= H // 8
-        assert (p["consumer_warps"] + 1) * p["ctas_per_sm"] <= 65536 // (72 * 32)
+        if p["consumer_warps"] <= 8:
+            assert (p["consumer_warps"] + 1) * p["ctas_per_sm"] <= 65536 // (72 * 32)
+        else:
+            assert p["chunks_per_lane"] in (2, 3, 4) and p["threads"] == 544
 
 
 def test_workspace_grows_with_t(lib):
@@ -291,9 +298,10 @@ def test_set_policy(lib):
 
 
 def test_set_policy_backward_sixteen_warps(lib):
-    # the backward ops take up to 16 consumer warps (one CTA per SM); the forward ops do not
+    # the backward ops and the fused quant take up to 16 consumer warps (one CTA per SM); the
+    # forward ops do not
     with pytest.raises(rmsn.RmsnError):
-        rmsn.rmsn_set_policy(rmsn.OP_FUSED_QUANT, consumer_warps=16)
+        rmsn.rmsn_set_policy(rmsn.OP_FWD, consumer_warps=16)
     with pytest.raises(rmsn.RmsnError):
         rmsn.rmsn_set_policy(rmsn.OP_BWD, consumer_warps=32)
     with pytest.raises(rmsn.RmsnError):

@@ -196,8 +196,10 @@ def test_bwd_t0_zeroes_dw():
 
 
 # ---------------------------------------------------------- fused add + norm + quant
+# (the last five: one CTA of 16 warps per SM, two stages up to H 12288, one above)
 FUSED_SHAPES = [(1, 128), (2, 256), (7, 384), (63, 1024), (65, 2048), (129, 4096),
-                (257, 5120), (31, 6144), (5, 16384), (2047, 4096)]
+                (257, 5120), (31, 6144), (2047, 4096), (301, 8320), (333, 10240),
+                (1000, 12288), (77, 14336), (5, 16384)]
 
 
 @pytest.mark.parametrize("T,H", FUSED_SHAPES)
