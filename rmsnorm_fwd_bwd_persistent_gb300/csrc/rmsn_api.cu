@@ -264,10 +264,12 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
     if (grid < 1) grid = 1;
     L->nw = nw;
     L->nch = nch;
-    // the backward takes bf16 rows of three vectors per lane one at a time when the lanes'
-    // third vectors are at least 3/4 full (measured on GB300: at 2.5 vectors per lane
-    // (H = 5120) pairs are 15% faster, at 3 (H = 6144) single rows 3-9% faster)
-    L->single = is_bwd && x_dt == RMSN_BF16 && nch == 3 && 4 * nvec >= 11 * 32 * (int64_t)nw;
+    // the backward takes bf16 rows of three vectors per lane one at a time with 16 warps, and
+    // with fewer when the lanes' third vectors are at least 3/4 full (measured on GB300: with
+    // 8 warps at 2.5 vectors per lane (H = 5120) pairs are 15% faster, at 3 (H = 6144) single
+    // rows 3-9% faster; with 16 warps single rows are 4-10% faster at H 8704-10240)
+    L->single = is_bwd && x_dt == RMSN_BF16 && nch == 3 &&
+                (nw == 16 || 4 * nvec >= 11 * 32 * (int64_t)nw);
     L->stages = (int)stages;
     L->ctas_per_sm = cps;
     L->sms = sms;

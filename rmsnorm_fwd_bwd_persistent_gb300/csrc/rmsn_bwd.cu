@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < NP; ++i) hi[c][i] = lo[c][i] = f2_splat(0.f);
 
-    // SINGLE (bf16 rows of three vectors per lane, nearly all lanes full): rows go one at a
+    // SINGLE (bf16 rows of three vectors per lane: 16 warps, or nearly all lanes full): rows go one at a
     // time, so one row's x and dy fit in registers beside the accumulators (a pair's would
     // not, in 128 registers), and every dw term is added with TwoSum whatever `compensated`
     // says.
