@@ -139,9 +139,12 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_bwd_kernel(BwdArgs a) {
     // says.
     // KEEP: pass 1 keeps the rows' x and dy vectors in registers for pass 2, so their
     // stages are released before the barrier and the whole ring can be in flight during
-    // pass 2.  Otherwise (long rows) pass 2 reads them from the stages again.
+    // pass 2 (up to two vectors per lane; fp32 rows, whose vectors hold four elements, up to
+    // three: measured on GB300 1.05-1.36x faster than re-reading, H 2560-6144, except fp32
+    // H 3072 at T = 65536, 3% slower).  Otherwise (long rows) pass 2 reads them from the
+    // stages again.
     static_assert(!SINGLE || NCH == 3, "single-row mode is compiled for three vectors per lane");
-    constexpr bool KEEP = NCH <= 2 || SINGLE;
+    constexpr bool KEEP = NCH <= 2 || SINGLE || (std::is_same<TX, float>::value && NCH == 3);
     uint4 xr[2][NCH], dr[2][NCH];
 
     // Rows go in pairs (r0 = row k in stage s0, r1 = row k+1 in stage s1; the CTA's last row

@@ -43,7 +43,9 @@ GEOMETRIES = [
     (400, 9216, BF, F32, 16, 3, 1),   # rows one at a time with 16 warps (third vector 1/4 full)
     (400, 12288, BF, F32, 16, 3, 1),  # rows one at a time with 16 warps
     (700, 384, F32, F32, 2, 2, 8),
-    (600, 2560, F32, BF, 8, 3, 2),
+    (600, 2560, F32, BF, 8, 3, 2),    # fp32 rows of three vectors per lane: pairs kept in registers
+    (300, 5120, F32, F32, 16, 3, 1),
+    (450, 6144, F32, BF, 16, 3, 1),
     (600, 3584, F32, F32, 8, 4, 2),
 ]
 IDS = [f"T{g[0]}-H{g[1]}-{'bf16' if g[2] == BF else 'fp32'}" for g in GEOMETRIES]
