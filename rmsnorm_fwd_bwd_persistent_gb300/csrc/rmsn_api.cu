@@ -192,6 +192,12 @@ int plan(int op, int64_t T, int64_t H, int x_dt, int w_dt, int sms, int64_t smem
                 nb * (kWarpsPerSm / nb) >= 14 && (8 * nvec <= 5 * lanes || T >= 16384))
                 nw = (int)nb;
         }
+        // short backward rows (1 or 2 warps) over short strips (fewer than 8 rows per chunk
+        // at 16 / nw CTAs per SM): twice the warps in half the CTAs, so half as many chunk
+        // partials to write and reduce.  Measured on GB300 (bf16, fp32 w): H 512 at T = 4096 /
+        // 8192 / 16384 24.7 -> 16.6 / 25.8 -> 19.3 / 29.0 -> 25.1 us, H 256 at T = 8192 21.3 ->
+        // 17.4, H 1024 at T = 4096 20.6 -> 18.0; at 13 or more rows per chunk the plan is best
+        if (is_bwd && nw <= 2 && T < 8 * (int64_t)sms * (kWarpsPerSm / nw)) nw *= 2;
     }
     const int64_t need = cdiv(nvec, 32 * nw);
     int nch = 0;

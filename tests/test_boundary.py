@@ -207,6 +207,20 @@ def test_plan_backward_warps_not_a_power_of_two(lib):
     assert seen == {3, 5, 7}
 
 
+def test_plan_backward_narrow_rows_over_short_strips(lib):
+    # rows the plan gives 1 or 2 warps take twice the warps in half the CTAs while a chunk
+    # would hold fewer than 8 rows (T < 8 * SMs * 16 / warps)
+    for H, xd, long_geom, short_geom in [(512, 1, (1, 16), (2, 8)), (1024, 1, (2, 8), (4, 4)),
+                                         (256, 0, (1, 16), (2, 8)), (4096, 1, (8, 2), (8, 2))]:
+        nw = long_geom[0]
+        limit = 8 * SM * (16 // nw)
+        for op in (rmsn.OP_BWD, rmsn.OP_BWD_RESIDUAL):
+            a = rmsn.rmsn_plan(op, limit, H, xd, 0)
+            b = rmsn.rmsn_plan(op, limit - 1, H, xd, 0)
+            assert (a["consumer_warps"], a["ctas_per_sm"]) == long_geom
+            assert (b["consumer_warps"], b["ctas_per_sm"]) == short_geom
+
+
 def test_plan_backward_warps_not_a_power_of_two_by_strip_length(lib):
     # rows the power of two fills to more than 5/8 (bf16 H 1536, 3584) change only over long
     # strips (T >= 16384); rows it fills to at most 5/8 (bf16 H 2304-2560, fp32 H 1280) at any T

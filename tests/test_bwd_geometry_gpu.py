@@ -2,7 +2,7 @@
 above the small-T route, so the deterministic calls run the strip kernel and the column
 reduce):
 4 CTAs of 4 warps, 5 of 3, 3 of 5 and 2 of 7 (rows that fill those warps at two vectors
-per lane), 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
+per lane), narrow rows over short strips with twice the warps in half the CTAs, 2 CTAs of 8 warps with rows in pairs (two and three vectors per lane),
 2 CTAs of 8 warps with rows one at a time (bf16, about three vectors per lane) and one CTA
 of 16 warps (rows of at least 1024 vectors; bf16 rows of three vectors per lane one at a
 time), each against the FP64 oracle, with plain and TwoSum-compensated dW, for rmsnorm_bwd and rmsnorm_bwd_residual (FlashInfer PR #5741
@@ -38,11 +38,13 @@ GEOMETRIES = [
     (300, 16384, BF, F32, 16, 4, 1),
     (513, 4096, F32, F32, 16, 2, 1),
     (300, 8192, F32, BF, 16, 4, 1),
-    (700, 384, BF, F32, 1, 2, 16),
+    (20000, 384, BF, F32, 1, 2, 16),
+    (700, 384, BF, F32, 2, 1, 8),     # short strip: twice the warps, half the CTAs
     (500, 7168, BF, BF, 8, 4, 2),
     (400, 9216, BF, F32, 16, 3, 1),   # rows one at a time with 16 warps (third vector 1/4 full)
     (400, 12288, BF, F32, 16, 3, 1),  # rows one at a time with 16 warps
-    (700, 384, F32, F32, 2, 2, 8),
+    (10000, 384, F32, F32, 2, 2, 8),
+    (700, 384, F32, F32, 4, 1, 4),    # short strip
     (600, 2560, F32, BF, 8, 3, 2),    # fp32 rows of three vectors per lane: pairs kept in registers
     (300, 5120, F32, F32, 16, 3, 1),
     (450, 6144, F32, BF, 16, 3, 1),
